@@ -1,0 +1,507 @@
+#!/usr/bin/env python
+"""Benchmark of the paged stream-attention cache on the LingBot-Map-shaped stream.
+
+Workload (one "step"): a 512-frame stream, 256 patch + 6 special tokens per
+frame, page_size 256, 8 scale frames, 64-frame window, special pages of
+42 x 6 tokens, 16 heads x 64, bf16, every frame a keyframe. Per frame:
+append (pop pages + scatter K/V), attend (visible table + paged attention of
+the frame's 262 queries), evict (window page back to the free list). Each
+step starts from an empty stream (pkv_stream_reset).
+
+Metric: frame-steps/s (whole job), with attention TFLOP/s against the bf16
+tensor roofline. Inputs (q, k, v for all 512 frames, 824 MB) are resident in
+HBM before timing; each step reads its own 824 MB (> L2).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs one independent replica per GPU (the stream does not shard; no
+collective on the data path); value = frames of all ranks / max time.
+"""
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "frame-steps/s and attn TFLOP/s (bf16 paged stream attn) vs GB300 roofline"
+UNIT = "frame-steps/s"
+WORKLOAD_NAME = "lingbot-1layer-512f-256p+6s-16x64-S8-W64"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--mode", choices=["graph", "eager"], default="graph")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+def workload():
+    from synth import WORKLOADS
+    return WORKLOADS["lingbot"]
+
+
+def config_dict(w):
+    return {"workload": WORKLOAD_NAME, "frames_per_step": w.frames, "tokens_per_frame": w.frame_tokens,
+            "heads": w.heads, "head_dim": w.head_dim, "page_size": w.page_size, "num_scale": w.num_scale,
+            "window": w.window, "special_frames_per_page": w.page_size // w.n_special,
+            "keyframe_interval": 1, "layers": 1, "pool_pages": w.pool_pages,
+            "l2": "inputs larger than L2: each step reads 824 MB of q/k/v; the ~85 MB of visible "
+                  "pages stay L2-resident across frames, as in a one-layer stream"}
+
+
+def frame_flops(w, n_kv):
+    return 4.0 * w.frame_tokens * n_kv * w.head_dim * w.heads
+
+
+def visible_tokens(w, t):
+    """Visible tokens while frame t attends (scale + window patches + specials)."""
+    patch_frames = min(t + 1, w.num_scale) + min(max(t + 1 - w.num_scale, 0), w.window)
+    return patch_frames * w.n_patch + (t + 1) * w.n_special
+
+
+# ----------------------------------------------------------------- dist
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return dist
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if self.proc is None or not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- peaks
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def attend_traffic_per_launch():
+    """DRAM bytes per attend launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "attend_lingbot_ncu.md")
+    src = os.path.join(ROOT, "paged_kv_cache_build_gb300", "csrc", "pkv_attend.cu")
+    if not os.path.exists(path):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != digest:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------ CPU oracle
+def _visible_input_lookup(w):
+    """K/V of a frame for the oracle's gather, generated once. At the last frame
+    only the scale and window frames' patch tokens are visible, so the other
+    frames get their special tokens only (the rest is never read)."""
+    import numpy as np
+    from synth import TENSOR_K, TENSOR_V, frame_tensor
+    last = w.frames - 1
+    cache = {}
+
+    def lookup(s, f, layer):
+        if (s, f) not in cache:
+            if f < w.num_scale or f > last - w.window:
+                cache[(s, f)] = tuple(frame_tensor(0, w.index, s, layer, f, t, w.frame_tokens,
+                                                   w.heads, 64) for t in (TENSOR_K, TENSOR_V))
+            else:
+                out = []
+                for t in (TENSOR_K, TENSOR_V):
+                    a = np.zeros((w.frame_tokens, w.heads, 64), np.uint16)
+                    a[w.n_patch:] = frame_tensor(0, w.index, s, layer, f, t, w.n_special, w.heads,
+                                                 64, token0=w.n_patch)
+                    out.append(a)
+                cache[(s, f)] = tuple(out)
+        return cache[(s, f)]
+    return lookup
+
+
+def oracle_sample(w, seconds, rank_tag=0):
+    """The CPU oracle as it stands on a bounded sample of the workload: the
+    metadata state machine over the whole stream plus fp64 attention of the
+    last frames (steady state, 21.5k visible tokens) until `seconds` pass."""
+    from oracle import PagedCacheOracle, StreamConfig, attend_fp64, gather_visible
+    from synth import TENSOR_Q, frame_tensor
+
+    lookup = _visible_input_lookup(w)
+
+    ora = PagedCacheOracle(w.pool_pages, w.page_size)
+    sid = ora.open_stream(StreamConfig(mode="frame", num_scale=w.num_scale, window=w.window,
+                                       n_patch=w.n_patch, n_special=w.n_special))
+    for t in range(w.frames - 1):
+        ora.append_frame(sid, t, w.frame_tokens)
+        ora.evict_window(sid)
+    # inputs of the sampled frames are generated before timing
+    t_last = w.frames - 1
+    for f in range(w.frames):
+        lookup(sid, f, 0)
+    q = frame_tensor(0, w.index, sid, 0, t_last, TENSOR_Q, w.frame_tokens, w.heads, 64, w.q_scale)
+    ora.append_frame(sid, t_last, w.frame_tokens)
+    n_frames, flops = 0, 0.0
+    t0 = time.perf_counter()
+    while True:
+        k, v = gather_visible(ora.visible_tokens(sid), 0, lookup)
+        attend_fp64(q, k, v, w.sm_scale)
+        n_frames += 1
+        flops += frame_flops(w, k.shape[0])
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    threads = int(os.environ.get("OMP_NUM_THREADS", cores))
+    return {"value": n_frames / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "gflops_fp64": flops / el / 1e9,
+            "sample": f"fp64 numpy oracle: metadata state machine over all 512 frames (untimed), then "
+                      f"gather + softmax attention of steady-state frame {t_last} (21,504 visible "
+                      f"tokens, 262 queries, 16 heads) repeated {n_frames}x in {el:.1f} s"}
+
+
+# ------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = dist_init(world, "nccl")
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_cache_build_gb300 import PagedKVCache, frame_stream_cfg, kernel_launches, synth_fill
+    from synth import TENSOR_K, TENSOR_Q, TENSOR_V
+
+    w = workload()
+    F, T, H, D = w.frames, w.frame_tokens, w.heads, w.head_dim
+    q = torch.empty((F, T, H, D), dtype=torch.bfloat16, device=device)
+    k = torch.empty_like(q)
+    v = torch.empty_like(q)
+    out = torch.empty_like(q)
+    synth_fill(q, 0, w.index, rank % 64, 0, 0, TENSOR_Q, 0, w.q_scale)
+    synth_fill(k, 0, w.index, rank % 64, 0, 0, TENSOR_K)
+    synth_fill(v, 0, w.index, rank % 64, 0, 0, TENSOR_V)
+
+    cache = PagedKVCache(w.pool_pages, w.page_size, H, D)
+    sid = cache.open_stream(frame_stream_cfg(w.num_scale, w.window, w.n_patch, w.n_special))
+    lib, h = cache.lib, cache.h
+    fb = T * H * D * 2
+    qp = [ctypes.c_void_p(q.data_ptr() + t * fb) for t in range(F)]
+    kp = [ctypes.c_void_p(k.data_ptr() + t * fb) for t in range(F)]
+    vp = [ctypes.c_void_p(v.data_ptr() + t * fb) for t in range(F)]
+    op = [ctypes.c_void_p(out.data_ptr() + t * fb) for t in range(F)]
+    scale = ctypes.c_float(w.sm_scale)
+
+    def check(st):
+        if st != 0:
+            raise RuntimeError(lib.pkv_last_error(h).decode())
+
+    def step(stream_ptr, events=None):
+        check(lib.pkv_stream_reset(h, sid, stream_ptr))
+        for t in range(F):
+            check(lib.pkv_append_frame(h, sid, 0, kp[t], vp[t], T, stream_ptr))
+            if events is not None:
+                events[t][0].record()
+            check(lib.pkv_attend(h, qp[t], T, sid, 0, op[t], scale, stream_ptr))
+            if events is not None:
+                events[t][1].record()
+            check(lib.pkv_evict_window(h, sid, stream_ptr))
+
+    cur = lambda: ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)  # noqa: E731
+    for _ in range(max(args.warmup, 3)):
+        step(cur())
+    torch.cuda.synchronize()
+    cache.sync()
+
+    graph = None
+    if args.mode == "graph":
+        graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graph, stream=s):
+                step(ctypes.c_void_p(s.cuda_stream))
+        torch.cuda.current_stream().wait_stream(s)
+        graph.replay()
+        torch.cuda.synchronize()
+        cache.sync()
+
+    # ---- main timed region
+    launches0 = kernel_launches()
+    per_step_launches = None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        e0.record()
+        for _ in range(args.steps):
+            if graph is not None:
+                graph.replay()
+            else:
+                step(cur())
+        e1.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(ms, world, device)
+    cache.sync()
+
+    # kernels per step, counted on one eager step (a graph replays the same launches)
+    l0 = kernel_launches()
+    step(cur())
+    torch.cuda.synchronize()
+    per_step_launches = kernel_launches() - l0
+    gpu_launches = per_step_launches * args.steps
+
+    # ---- attend launches timed with events around each call (same kernels)
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(F)]
+    att_ms, att_flops, steady_ms, steady_flops = 0.0, 0.0, 0.0, 0.0
+    n_att_steps = min(args.steps, 5)
+    for _ in range(n_att_steps):
+        step(cur(), events)
+        torch.cuda.synchronize()
+        for t in range(F):
+            d = events[t][0].elapsed_time(events[t][1])
+            fl = frame_flops(w, visible_tokens(w, t))
+            att_ms += d
+            att_flops += fl
+            if t >= w.num_scale + w.window - 1:
+                steady_ms += d
+                steady_flops += fl
+    cache.sync()
+    attn_tflops = att_flops / (att_ms * 1e-3) / 1e12
+    steady_tflops = steady_flops / (steady_ms * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers (pinned), eager calls
+    hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    hk = torch.empty_like(hq, pin_memory=True)
+    hv = torch.empty_like(hq, pin_memory=True)
+    ho = torch.empty_like(hq, pin_memory=True)
+    hq.copy_(q)
+    hk.copy_(k)
+    hv.copy_(v)
+    stage = [torch.empty((T, H, D), dtype=torch.bfloat16, device=device) for _ in range(4)]
+    sq, sk, sv, so = [ctypes.c_void_p(x.data_ptr()) for x in stage]
+    n_e2e = min(args.steps, 5)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall = time.perf_counter()
+    f0.record()
+    for _ in range(n_e2e):
+        sp = cur()
+        check(lib.pkv_stream_reset(h, sid, sp))
+        for t in range(F):
+            stage[0].copy_(hq[t], non_blocking=True)
+            stage[1].copy_(hk[t], non_blocking=True)
+            stage[2].copy_(hv[t], non_blocking=True)
+            check(lib.pkv_append_frame(h, sid, 0, sk, sv, T, sp))
+            check(lib.pkv_attend(h, sq, T, sid, 0, so, scale, sp))
+            check(lib.pkv_evict_window(h, sid, sp))
+            ho[t].copy_(stage[3], non_blocking=True)
+    f1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    e2e_ms = max(f0.elapsed_time(f1), wall * 1e3)
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
+    cache.sync()
+    ok = torch.equal(ho.to(device), out)   # same inputs, same kernels: identical outputs
+
+    if rank != 0:
+        return
+    peaks, peak_kind = measured_peaks()
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    frames_total = F * args.steps * world
+    value = frames_total / (ms_max * 1e-3)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_max / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "impl": "ours", "mode": args.mode,
+        "config": config_dict(w),
+        "attn_tflops": round(attn_tflops, 2), "attn_tflops_steady": round(steady_tflops, 2),
+        "attn_us_per_frame": round(att_ms * 1e3 / (F * n_att_steps), 3),
+        "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(attn_tflops / peak, 4),
+                     "traffic": attend_traffic_per_launch(),
+                     "peak_source": f"bf16_tflops_sustained ({peak_kind}); kernel: pkv_attend call "
+                                    f"(table + attention + split combine), useful flops "
+                                    f"4*262*N_kv*64*16 per frame, every frame of the stream"},
+        "e2e": {"value": round(F * n_e2e * world / (e2e_ms * 1e-3), 2), "unit": UNIT,
+                "h2d_bytes_per_step": 3 * F * fb, "d2h_bytes_per_step": F * fb,
+                "outputs_match_device_run": bool(ok)},
+        "gpu_launches": int(gpu_launches),
+        "launches_per_step": int(per_step_launches),
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------- reference arm
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is one steady-state frame
+    of the same workload (a bounded sample), timed on the host cores."""
+    world, rank, _ = dist_setup()
+    if world > 1:
+        dist = dist_init(world, "gloo")
+        dist.barrier()
+        if rank != 0:
+            return
+    w = workload()
+    from oracle import PagedCacheOracle, StreamConfig, attend_fp64, gather_visible
+    from synth import TENSOR_Q, frame_tensor
+
+    lookup = _visible_input_lookup(w)
+
+    ora = PagedCacheOracle(w.pool_pages, w.page_size)
+    sid = ora.open_stream(StreamConfig(mode="frame", num_scale=w.num_scale, window=w.window,
+                                       n_patch=w.n_patch, n_special=w.n_special))
+    for t in range(w.frames - 1):
+        ora.append_frame(sid, t, w.frame_tokens)
+        ora.evict_window(sid)
+    t_last = w.frames - 1
+    for f in range(w.frames):
+        lookup(sid, f, 0)
+    q = frame_tensor(0, w.index, sid, 0, t_last, TENSOR_Q, w.frame_tokens, w.heads, 64, w.q_scale)
+
+    def one():
+        ora.append_frame(sid, t_last, w.frame_tokens)
+        k, v = gather_visible(ora.visible_tokens(sid), 0, lookup)
+        attend_fp64(q, k, v, w.sm_scale)
+        ora.rollback_last_frame(sid)
+
+    for _ in range(max(args.warmup, 1)):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    el = time.perf_counter() - t0
+    value = args.steps / el
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference", "config": config_dict(w),
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "one steady-state frame (frame 511: append, gather of 21,504 "
+                                       "visible tokens, fp64 attention of 262 queries x 16 heads, "
+                                       "rollback) per step"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,238 @@
+/*
+ * pkv.h - paged KV cache for streaming 3D reconstruction on one GB300 (sm_103a).
+ *
+ * What the library computes
+ * -------------------------
+ * "LingBot-Map Paged KV Cache: 3D reconstruction managed like LLM memory",
+ * section 2: each layer's KV is cut into fixed-size pages handed out from a free
+ * list. A stream's cache has three page types:
+ *   - scale pages: the patch tokens of the first num_scale frames, never evicted;
+ *   - sliding-window pages: the patch tokens of the most recent `window` frames;
+ *     a page that leaves the window goes straight back to the free list, where
+ *     the next frame reuses it;
+ *   - special pages: each frame's n_special special tokens (camera / register /
+ *     scale), appended floor(page_size / n_special) frames to a page (42 x 6 in a
+ *     256-slot page), never recycled.
+ * Attention runs over a visible page table built in the order scale -> window ->
+ * special; the fill of the last page is last_page_len. Section 3: a non-keyframe
+ * is appended, attended, then rolled back. Section 4: in windowed mode the cache
+ * is reset once per window of window_slots KV slots, and the last
+ * overlap_keyframes keyframes carry over into the next window.
+ *
+ * vLLM-Omni RFC "Reconstruction Engine" (issue 2727), sections 2.3 and 3.3:
+ * chunked sliding-window global attention. Frames are grouped in chunks of
+ * chunk_size; the current chunk's tokens attend over the KV of the most recent
+ * sliding_window_num chunks (itself included); the oldest chunk is then evicted.
+ *
+ * Conventions (every call)
+ * ------------------------
+ *  - Tensors q, k, v, out are caller-owned DEVICE buffers of bf16, layout
+ *    [tokens][heads][head_dim], contiguous, 16-byte aligned. Values must be finite.
+ *  - `cuda_stream` is a cudaStream_t (NULL = legacy default stream). Every call
+ *    that touches the device is asynchronous and ordered on that stream. All
+ *    calls on one handle must be issued on one CUDA stream, or ordered by the
+ *    caller: the handle's device metadata and scratch are shared by its calls.
+ *  - The library owns the page pool, the free list and all page-id metadata in
+ *    device memory (allocated by create / stream_open, freed by close / destroy).
+ *    The host keeps only counters, so argument, capacity (OOM) and call-order
+ *    (STATE) errors are detected before anything is launched: a call that
+ *    returns an error has changed nothing. Kernels that find an inconsistency
+ *    (a page id outside the pool) record it in a device error word instead of
+ *    faulting; pkv_sync reports it as PKV_ERR_DEVICE.
+ *  - Non-zero statuses come with a message from pkv_last_error.
+ *  - head_dim must be 64; page_size a multiple of 16 in [16, 256] that divides
+ *    or is divided by 64.
+ *  - There is no CPU fallback and no other backend.
+ *
+ * Pool layout (documented for callers that read the pool directly)
+ * ------------------------------------------------------------------
+ * pool[layer][page][kv][head][slot][64] bf16, kv = 0 for K, 1 for V. Inside each
+ * [slot][64] block (one 128-byte row per slot) the eight 16-byte chunks of a row
+ * are stored XOR-swizzled: logical chunk c of slot s sits at chunk (c ^ (s & 7)).
+ * This is the 128-byte-swizzled operand layout the tensor cores read, so a page
+ * block is copied into shared memory as-is. Every slot of a held page is either a
+ * valid token or zero.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pkv_ctx* pkv_t;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID = 1, /* bad argument or shape                                  */
+  PKV_ERR_OOM = 2,     /* the free list (or the stream table) cannot cover the call */
+  PKV_ERR_STATE = 3,   /* call order: e.g. rollback with nothing to roll back    */
+  PKV_ERR_CUDA = 4,    /* a CUDA runtime call failed                             */
+  PKV_ERR_TIMEOUT = 5, /* a bounded device wait gave up                          */
+  PKV_ERR_DEVICE = 6   /* a kernel recorded an inconsistency in the error word   */
+} pkv_status;
+
+enum { PKV_MODE_FRAME = 0, PKV_MODE_CHUNKED = 1 };
+
+/* Per-stream configuration. Fields of the other mode are ignored. */
+typedef struct {
+  int mode;              /* PKV_MODE_FRAME or PKV_MODE_CHUNKED                      */
+  /* frame mode (LingBot-Map) */
+  int num_scale;         /* scale frames kept forever (8)                           */
+  int window;            /* sliding-window frames, including the current one (64)   */
+  int n_patch;           /* patch tokens per frame; must equal page_size (256)      */
+  int n_special;         /* special tokens per frame (6)                            */
+  int window_slots;      /* windowed mode: KV slots (cached keyframes) per window; 0 = off */
+  int overlap_keyframes; /* keyframes carried into the next window; <= num_scale    */
+  /* chunked mode (VGGT RFC) */
+  int chunk_size;        /* frames per chunk (8)                                    */
+  int sliding_window_num;/* chunks visible, including the current one (4)           */
+  int tokens_per_frame;  /* tokens appended per frame (1374)                        */
+} pkv_stream_cfg;
+
+/* Create a cache of `pool_pages` pages of `page_size` slots for one layer.
+ * Equivalent to pkv_create_ex(pool_pages, page_size, heads, head_dim, 1, 64, out). */
+pkv_status pkv_create(int pool_pages, int page_size, int heads, int head_dim, pkv_t* out);
+
+/* Create with `layers` page sets (one per transformer layer; all layers share one
+ * page table, so a page id names the same page in every layer) and room for
+ * `max_streams` concurrent streams sharing the pool and its free list.
+ * Allocates layers*pool_pages*2*heads*page_size*head_dim bf16 (zeroed). The free
+ * list is a stack that initially hands out pages 0, 1, 2, ... */
+pkv_status pkv_create_ex(int pool_pages, int page_size, int heads, int head_dim, int layers,
+                         int max_streams, pkv_t* out);
+
+/* Free everything. Synchronises the device first. NULL is accepted. */
+pkv_status pkv_destroy(pkv_t h);
+
+/* Open a stream; *stream_id receives the lowest unused id. Allocates the stream's
+ * page-id lists on the device (synchronously). */
+pkv_status pkv_stream_open(pkv_t h, const pkv_stream_cfg* cfg, int* stream_id);
+
+/* Close a stream: its pages go back on the free stack (frame mode: scale pages,
+ * window pages oldest first, then special pages in order; chunked mode: chunks
+ * oldest first, pages in order). */
+pkv_status pkv_stream_close(pkv_t h, int stream_id, void* cuda_stream);
+
+/* Return every page of the stream to the free stack (in pkv_stream_close's
+ * order) and clear its counters, keeping the stream open and its device lists
+ * allocated: the stream starts over as if just opened. No allocation and no
+ * synchronisation, so it can sit inside a captured CUDA graph. */
+pkv_status pkv_stream_reset(pkv_t h, int stream_id, void* cuda_stream);
+
+/* Append one frame's K and V ("LingBot-Map Paged KV Cache", section 2; RFC
+ * section 3.3 "KV Cache append").
+ * k, v: device bf16 [n_tokens][heads][head_dim], tokens in frame order (frame
+ * mode: n_patch patch tokens then n_special special tokens).
+ * layer == 0 starts a new frame: pages are popped from the free list (frame mode:
+ * the patch page first, then a new special page when the current one holds
+ * floor(page_size/n_special) frames; chunked mode: as many pages as the chunk's
+ * packed tokens need, a new chunk starting on a new page) and the tokens are
+ * scattered into their slots. layer > 0 writes the same slots of that layer's
+ * page set and must follow layer 0 of the same frame.
+ * Errors: INVALID (shape / layer), OOM (too few free pages), STATE (frame mode:
+ * the window already holds `window` pages; chunked: the chunk is full or the
+ * window holds sliding_window_num chunks; layer > 0 without a pending frame). */
+pkv_status pkv_append_frame(pkv_t h, int stream_id, int layer, const void* k, const void* v,
+                            int n_tokens, void* cuda_stream);
+
+/* Append one frame to each of `n` frame-mode streams (n <= 32) in one launch, in
+ * the order given: stream i pops its pages after streams 0..i-1 (an exclusive
+ * warp scan of the page needs gives each stream its place on the free stack).
+ * stream_ids, k, v are HOST arrays of n entries; k[i], v[i] are device pointers.
+ * The batch is validated as a whole: on error nothing is appended. */
+pkv_status pkv_append_frames(pkv_t h, int n, const int* stream_ids, int layer,
+                             const void* const* k, const void* const* v, int n_tokens,
+                             void* cuda_stream);
+
+/* Undo the last append (section 3: a non-keyframe is appended, attended, then
+ * rolled back). Pages it popped are pushed back in reverse order, so the free
+ * stack, the page lists and every valid slot are exactly as before the append.
+ * Errors: STATE if no append is pending (already rolled back, or committed by
+ * pkv_evict_window). */
+pkv_status pkv_rollback_last_frame(pkv_t h, int stream_id, void* cuda_stream);
+
+/* Commit the pending frame and evict (section 2; RFC 3.3 "evict oldest chunk").
+ * Frame mode: window pages beyond window-1 go back on the free stack, oldest
+ * first, so the next frame reuses them; no KV bytes move. In windowed mode, once
+ * the stream holds window_slots cached keyframes, the window is reset (section 4):
+ * the last overlap_keyframes held frames become the new window's scale frames
+ * (their patch pages stay in place; their special tokens are copied, for every
+ * layer, into freshly popped special pages) and all other pages are freed.
+ * Chunked mode: closes the current chunk and frees the oldest chunks' pages until
+ * sliding_window_num-1 chunks remain.
+ * Errors: OOM if a reset cannot pop its special page. */
+pkv_status pkv_evict_window(pkv_t h, int stream_id, void* cuda_stream);
+
+/* Write the visible page table (section 2, build_visible_page_table): page ids in
+ * the order scale -> window (oldest first) -> special (allocation order); chunked
+ * mode: chunks oldest first, pages in order.
+ * d_idx, d_len: device int32[capacity] receiving page ids and valid slot counts;
+ * d_n, d_last_page_len: device int32 scalars (may be NULL) receiving the entry
+ * count and the last entry's length. Errors: INVALID if capacity is too small. */
+pkv_status pkv_build_visible_page_table(pkv_t h, int stream_id, int32_t* d_idx, int32_t* d_len,
+                                        int capacity, int32_t* d_n, int32_t* d_last_page_len,
+                                        void* cuda_stream);
+
+/* Frame-mode attention (sections 1-2): for every query row i < n_q and head h,
+ * out[i][h] = softmax(sm_scale * q[i][h] . K^T) V over every valid slot of the
+ * stream's visible pages (no mask besides page validity: bidirectional).
+ * q, out: device bf16 [n_q][heads][64]; fp32 accumulation and softmax.
+ * sm_scale <= 0 means 1/sqrt(head_dim). Errors: STATE if nothing is visible. */
+pkv_status pkv_attend(pkv_t h, const void* q, int n_q, int stream_id, int layer, void* out,
+                      float sm_scale, void* cuda_stream);
+
+/* Chunked-mode attention (RFC 2.3 / 3.3): the current chunk's n_q tokens (n_q
+ * must equal the tokens appended to the open chunk) attend over the visible
+ * chunks. Same layouts and numerics as pkv_attend. */
+pkv_status pkv_attend_chunked(pkv_t h, const void* q, int n_q, int stream_id, int layer,
+                              void* out, float sm_scale, void* cuda_stream);
+
+/* Wait for `cuda_stream` and report the device error word (PKV_ERR_DEVICE) or a
+ * pending CUDA error (PKV_ERR_CUDA). */
+pkv_status pkv_sync(pkv_t h, void* cuda_stream);
+
+/* Host-side counts of the stream's visible table (no device access). */
+pkv_status pkv_visible_count(pkv_t h, int stream_id, int* n_pages, int* n_tokens);
+
+/* Number of free pages (host mirror of the free-stack depth). */
+pkv_status pkv_free_pages(pkv_t h, int* n_free);
+
+/* Debug / test export (synchronises the device). Writes int32 words to host_buf:
+ *   [0] free-stack depth F, [1..F] free stack bottom to top,
+ *   then the stream's visible table: n, idx[0..n), len[0..n),
+ *   then mode-specific counters: frame mode {n_scale, n_window, n_special, sp_len,
+ *   kept, pending}; chunked mode {n_chunks, open, pending, tokens of each chunk}.
+ * cap_words is the capacity of host_buf; *used_words receives the count. */
+pkv_status pkv_export_state(pkv_t h, int stream_id, int32_t* host_buf, size_t cap_words,
+                            size_t* used_words);
+
+/* Debug / test read of one page's K (kv = 0) or V (kv = 1) of one layer, copied to
+ * host_dst as plain bf16 [heads][page_size][64] (un-swizzled). Synchronous. */
+pkv_status pkv_read_page(pkv_t h, int layer, int page, int kv, void* host_dst);
+
+/* Synthetic input generator (not part of the cache): fills dst, a device bf16
+ * array [n_frames][n_tokens][heads][head_dim], with the counter-based ~N(0,1)
+ * values of frames frame0 .. frame0+n_frames-1: splitmix64 of the packed key
+ * (seed, workload, stream, layer, frame, tensor, token0+t, head, d), four 16-bit
+ * uniforms summed, centred, scaled by sqrt(3)*2^-16 in fp32, times `scale` (a
+ * power of two), rounded to bf16. */
+pkv_status pkv_synth_fill(void* dst, int n_frames, int n_tokens, int heads, int head_dim,
+                          int seed, int workload, int stream, int layer, int frame0, int tensor,
+                          int token0, float scale, void* cuda_stream);
+
+/* Kernels this library has launched in the calling process so far (all handles). */
+unsigned long long pkv_kernel_launches(void);
+
+/* Message of the last error on this handle ("" if none). h may be NULL for
+ * errors of pkv_create. */
+const char* pkv_last_error(pkv_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

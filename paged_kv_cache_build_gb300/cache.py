@@ -1,0 +1,179 @@
+"""Python binding of libpkv: argument marshalling over the C ABI, nothing more.
+
+Tensors are torch CUDA tensors (bf16, contiguous, [tokens][heads][64]); every
+call is ordered on torch's current CUDA stream unless a stream is given. All
+computation runs in the library's kernels.
+"""
+
+import ctypes
+
+import torch
+
+from ._lib import PkvError, StreamCfg, check, load
+
+MODE_FRAME = 0
+MODE_CHUNKED = 1
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _bf16_ptr(t, name):
+    if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def frame_stream_cfg(num_scale, window, n_patch, n_special, window_slots=0, overlap_keyframes=0):
+    return StreamCfg(MODE_FRAME, num_scale, window, n_patch, n_special, window_slots,
+                     overlap_keyframes, 0, 0, 0)
+
+
+def chunked_stream_cfg(chunk_size, sliding_window_num, tokens_per_frame):
+    return StreamCfg(MODE_CHUNKED, 0, 0, 0, 0, 0, 0, chunk_size, sliding_window_num,
+                     tokens_per_frame)
+
+
+class PagedKVCache:
+    """A page pool (per layer) with its free list, shared by up to max_streams streams."""
+
+    def __init__(self, pool_pages, page_size, heads, head_dim=64, layers=1, max_streams=64):
+        self.lib = load()
+        self.pool_pages, self.page_size, self.heads, self.head_dim = pool_pages, page_size, heads, head_dim
+        self.layers = layers
+        h = ctypes.c_void_p()
+        check(self.lib.pkv_create_ex(pool_pages, page_size, heads, head_dim, layers, max_streams,
+                                     ctypes.byref(h)), None)
+        self.h = h
+
+    def close(self):
+        if self.h is not None and self.h.value:
+            self.lib.pkv_destroy(self.h)
+        self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _check(self, status):
+        check(status, self.h)
+
+    # -------------------------------------------------------------- streams
+    def open_stream(self, cfg):
+        sid = ctypes.c_int(-1)
+        self._check(self.lib.pkv_stream_open(self.h, ctypes.byref(cfg), ctypes.byref(sid)))
+        return sid.value
+
+    def close_stream(self, sid, stream=None):
+        self._check(self.lib.pkv_stream_close(self.h, sid, _stream_ptr(stream)))
+
+    def reset_stream(self, sid, stream=None):
+        self._check(self.lib.pkv_stream_reset(self.h, sid, _stream_ptr(stream)))
+
+    def append_frame(self, sid, k, v, layer=0, stream=None):
+        self._check(self.lib.pkv_append_frame(self.h, sid, layer, _bf16_ptr(k, "k"), _bf16_ptr(v, "v"),
+                                              k.shape[0], _stream_ptr(stream)))
+
+    def append_frames(self, sids, ks, vs, layer=0, stream=None):
+        n = len(sids)
+        ids = (ctypes.c_int * n)(*sids)
+        kp = (ctypes.c_void_p * n)(*[_bf16_ptr(k, "k").value for k in ks])
+        vp = (ctypes.c_void_p * n)(*[_bf16_ptr(v, "v").value for v in vs])
+        self._check(self.lib.pkv_append_frames(self.h, n, ids, layer, kp, vp, ks[0].shape[0],
+                                               _stream_ptr(stream)))
+
+    def rollback_last_frame(self, sid, stream=None):
+        self._check(self.lib.pkv_rollback_last_frame(self.h, sid, _stream_ptr(stream)))
+
+    def evict_window(self, sid, stream=None):
+        self._check(self.lib.pkv_evict_window(self.h, sid, _stream_ptr(stream)))
+
+    def build_visible_page_table(self, sid, capacity=None, stream=None):
+        """Returns device int32 tensors (idx[n], len[n], n[1], last_page_len[1])."""
+        n_pages, _ = self.visible_count(sid)
+        cap = capacity if capacity is not None else max(1, n_pages)
+        dev = torch.device("cuda", torch.cuda.current_device())
+        idx = torch.empty(cap, dtype=torch.int32, device=dev)
+        lens = torch.empty(cap, dtype=torch.int32, device=dev)
+        n = torch.empty(1, dtype=torch.int32, device=dev)
+        last = torch.empty(1, dtype=torch.int32, device=dev)
+        self._check(self.lib.pkv_build_visible_page_table(
+            self.h, sid, ctypes.c_void_p(idx.data_ptr()), ctypes.c_void_p(lens.data_ptr()), cap,
+            ctypes.c_void_p(n.data_ptr()), ctypes.c_void_p(last.data_ptr()), _stream_ptr(stream)))
+        return idx[:n_pages], lens[:n_pages], n, last
+
+    def attend(self, q, sid, layer=0, out=None, sm_scale=0.0, stream=None):
+        if out is None:
+            out = torch.empty_like(q)
+        self._check(self.lib.pkv_attend(self.h, _bf16_ptr(q, "q"), q.shape[0], sid, layer,
+                                        _bf16_ptr(out, "out"), float(sm_scale), _stream_ptr(stream)))
+        return out
+
+    def attend_chunked(self, q, sid, layer=0, out=None, sm_scale=0.0, stream=None):
+        if out is None:
+            out = torch.empty_like(q)
+        self._check(self.lib.pkv_attend_chunked(self.h, _bf16_ptr(q, "q"), q.shape[0], sid, layer,
+                                                _bf16_ptr(out, "out"), float(sm_scale),
+                                                _stream_ptr(stream)))
+        return out
+
+    def sync(self, stream=None):
+        self._check(self.lib.pkv_sync(self.h, _stream_ptr(stream)))
+
+    # ---------------------------------------------------------------- state
+    def visible_count(self, sid):
+        n_pages, n_tokens = ctypes.c_int(), ctypes.c_int()
+        self._check(self.lib.pkv_visible_count(self.h, sid, ctypes.byref(n_pages), ctypes.byref(n_tokens)))
+        return n_pages.value, n_tokens.value
+
+    def free_pages(self):
+        n = ctypes.c_int()
+        self._check(self.lib.pkv_free_pages(self.h, ctypes.byref(n)))
+        return n.value
+
+    def export_state(self, sid):
+        """(free stack bottom..top, table idx, table len, counters) read from the device."""
+        cap = self.pool_pages * 4 + 1024
+        buf = (ctypes.c_int32 * cap)()
+        used = ctypes.c_size_t()
+        self._check(self.lib.pkv_export_state(self.h, sid, buf, cap, ctypes.byref(used)))
+        w = list(buf[:used.value])
+        f = w[0]
+        free = w[1:1 + f]
+        n = w[1 + f]
+        idx = w[2 + f:2 + f + n]
+        lens = w[2 + f + n:2 + f + 2 * n]
+        return free, idx, lens, w[2 + f + 2 * n:]
+
+    def read_page(self, page, kv, layer=0):
+        """One page's K (kv=0) or V (kv=1) as a host uint16 array [heads][page_size][64]."""
+        import numpy as np
+        out = np.empty((self.heads, self.page_size, self.head_dim), dtype=np.uint16)
+        self._check(self.lib.pkv_read_page(self.h, layer, page, kv, out.ctypes.data_as(ctypes.c_void_p)))
+        return out
+
+
+def kernel_launches():
+    """Kernels libpkv has launched in this process."""
+    return int(load().pkv_kernel_launches())
+
+
+def synth_fill(out, seed, workload, stream_id, layer, frame0, tensor, token0=0, scale=1.0, stream=None):
+    """Fill a device bf16 tensor [n_frames][n_tokens][heads][head_dim] (or
+    [n_tokens][heads][head_dim] for one frame) with the counter-based inputs."""
+    lib = load()
+    shape = out.shape if out.dim() == 4 else (1,) + tuple(out.shape)
+    n_frames, n_tokens, heads, head_dim = shape
+    check(lib.pkv_synth_fill(_bf16_ptr(out, "out"), n_frames, n_tokens, heads, head_dim, seed, workload,
+                             stream_id, layer, frame0, tensor, token0, float(scale), _stream_ptr(stream)))
+    return out
+
+
+__all__ = ["PagedKVCache", "PkvError", "frame_stream_cfg", "chunked_stream_cfg", "synth_fill",
+           "kernel_launches",
+           "MODE_FRAME", "MODE_CHUNKED"]

@@ -1,0 +1,913 @@
+// C-ABI entry points of libpkv: the handle, host-side counters and validation,
+// and the launches. See include/pkv.h for each call's contract.
+//
+// Split of responsibilities: the device holds the page pool, the free stack's
+// array and every stream's page-id lists; the host mirrors only counters (free
+// stack depth, list lengths, ring heads, special fill, chunk lengths). All
+// capacity and call-order checks run on the host before anything is launched,
+// so an error return leaves the cache untouched, and every kernel gets the
+// positions it reads and writes as arguments.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/pkv.h"
+#include "pkv_internal.cuh"
+
+using namespace pkv;
+
+namespace {
+
+struct Stream {
+  bool open = false;
+  pkv_stream_cfg cfg{};
+  // device lists (one allocation)
+  int32_t* d_mem = nullptr;
+  int32_t* d_scale = nullptr;
+  int32_t* d_window = nullptr;
+  int32_t* d_special = nullptr;
+  int32_t* d_chunks = nullptr;   // [sliding_window_num][ppc]
+  int32_t* d_tbl_idx = nullptr;
+  int32_t* d_tbl_len = nullptr;
+  int tbl_cap = 0;
+  // frame-mode counters
+  int f_sp = 0;
+  int n_scale = 0, win_head = 0, win_count = 0, n_special = 0, sp_len = 0, kept = 0;
+  bool pending = false;
+  bool u_to_scale = false, u_new_sp = false;
+  int u_sp_before = 0, u_sp_off = 0, u_patch_pos = 0;
+  // chunked-mode counters (by ring slot)
+  int ppc = 0;
+  int c_head = 0, n_chunks = 0;
+  bool c_open = false;
+  int c_len[kMaxChunks] = {0}, c_pages[kMaxChunks] = {0}, c_frames[kMaxChunks] = {0};
+  int u_n_new = 0, u_old_pages = 0, u_pos0 = 0, u_slot = 0;
+  bool u_new_chunk = false;
+};
+
+}  // namespace
+
+struct pkv_ctx {
+  int P = 0, Ps = 0, H = 0, D = 0, L = 0, max_streams = 0;
+  long long page_elems = 0;
+  uint16_t* d_pool = nullptr;
+  int32_t* d_free = nullptr;
+  int* d_err = nullptr;
+  int free_top = 0;
+  std::vector<Stream> streams;
+  float* d_scratch = nullptr;
+  size_t scratch_bytes = 0;
+  int num_sms = 0;
+  std::string last_error;
+};
+
+namespace {
+
+std::string g_create_error;
+
+pkv_status fail(pkv_t h, pkv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (h) h->last_error = buf;
+  else g_create_error = buf;
+  return st;
+}
+
+pkv_status cuda_fail(pkv_t h, cudaError_t e, const char* what) {
+  return fail(h, PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define PKV_CUDA(h, call)                                  \
+  do {                                                     \
+    cudaError_t e_ = (call);                               \
+    if (e_ != cudaSuccess) return cuda_fail((h), e_, #call); \
+  } while (0)
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline PoolView pool_view(pkv_t h, int layer) {
+  PoolView pv;
+  pv.base = h->d_pool + (long long)layer * h->P * h->page_elems;
+  pv.page_elems = h->page_elems;
+  pv.heads = h->H;
+  pv.page_size = h->Ps;
+  pv.pool_pages = h->P;
+  return pv;
+}
+
+pkv_status get_stream(pkv_t h, int sid, Stream** out) {
+  if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
+  if (sid < 0 || sid >= h->max_streams || !h->streams[sid].open)
+    return fail(h, PKV_ERR_INVALID, "stream %d is not open", sid);
+  *out = &h->streams[sid];
+  return PKV_OK;
+}
+
+inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Visible table size from the counters.
+void visible_counts(const pkv_ctx* h, const Stream& st, int* n_pages, int* n_tokens, int* last) {
+  if (st.cfg.mode == PKV_MODE_FRAME) {
+    const int np = st.n_scale + st.win_count + st.n_special;
+    int nt = (st.n_scale + st.win_count) * h->Ps;
+    if (st.n_special > 0) nt += (st.n_special - 1) * st.f_sp * st.cfg.n_special + st.sp_len;
+    *n_pages = np;
+    *n_tokens = nt;
+    *last = st.n_special > 0 ? st.sp_len : (np > 0 ? h->Ps : 0);
+  } else {
+    int np = 0, nt = 0, lst = 0;
+    for (int i = 0; i < st.n_chunks; ++i) {
+      const int slot = (st.c_head + i) % st.cfg.sliding_window_num;
+      np += st.c_pages[slot];
+      nt += st.c_len[slot];
+      lst = st.c_len[slot] - (st.c_pages[slot] - 1) * h->Ps;
+    }
+    *n_pages = np;
+    *n_tokens = nt;
+    *last = np > 0 ? lst : 0;
+  }
+}
+
+TableArgs table_args(pkv_t h, Stream& st, int32_t* idx, int32_t* len, int32_t* out_n,
+                     int32_t* out_last) {
+  TableArgs t;
+  std::memset(&t, 0, sizeof(t));
+  int np, nt, last;
+  visible_counts(h, st, &np, &nt, &last);
+  t.mode = st.cfg.mode;
+  t.n = np;
+  t.page_size = h->Ps;
+  t.pool_pages = h->P;
+  if (st.cfg.mode == PKV_MODE_FRAME) {
+    t.scale = st.d_scale;
+    t.n_scale = st.n_scale;
+    t.window = st.d_window;
+    t.win_head = st.win_head;
+    t.win_count = st.win_count;
+    t.win_cap = st.cfg.window;
+    t.special = st.d_special;
+    t.n_special = st.n_special;
+    t.sp_full_len = st.f_sp * st.cfg.n_special;
+    t.sp_last_len = st.sp_len;
+  } else {
+    t.n_chunks = st.n_chunks;
+    for (int i = 0; i < st.n_chunks; ++i) {
+      const int slot = (st.c_head + i) % st.cfg.sliding_window_num;
+      t.chunk_pages[i] = st.d_chunks + (long long)slot * st.ppc;
+      t.chunk_npages[i] = st.c_pages[slot];
+      t.chunk_len[i] = st.c_len[slot];
+    }
+  }
+  t.out_idx = idx;
+  t.out_len = len;
+  t.out_n = out_n;
+  t.out_last = out_last;
+  t.err = h->d_err;
+  return t;
+}
+
+pkv_status push_pages(pkv_t h, const PushSegment* segs, int n_seg, cudaStream_t s) {
+  int total = 0;
+  PushArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int i = 0; i < n_seg; ++i) {
+    if (segs[i].count <= 0) continue;
+    if (a.n_seg == kMaxSegments) return fail(h, PKV_ERR_INVALID, "too many page segments");
+    a.seg[a.n_seg++] = segs[i];
+    total += segs[i].count;
+  }
+  if (total == 0) return PKV_OK;
+  if (h->free_top + total > h->P) return fail(h, PKV_ERR_STATE, "free stack overflow");
+  a.free_stack = h->d_free;
+  a.top = h->free_top;
+  a.pool_pages = h->P;
+  a.err = h->d_err;
+  PKV_CUDA(h, launch_push(a, s));
+  h->free_top += total;
+  return PKV_OK;
+}
+
+PushSegment seg(const int32_t* src, int start, int count, int step = 1, int ring = 0) {
+  PushSegment g;
+  g.src = src;
+  g.start = start;
+  g.count = count;
+  g.step = step;
+  g.ring = ring;
+  return g;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+unsigned long long pkv_kernel_launches(void) { return pkv::launch_count(); }
+
+const char* pkv_last_error(pkv_t h) { return h ? h->last_error.c_str() : g_create_error.c_str(); }
+
+pkv_status pkv_create(int pool_pages, int page_size, int heads, int head_dim, pkv_t* out) {
+  return pkv_create_ex(pool_pages, page_size, heads, head_dim, 1, 64, out);
+}
+
+pkv_status pkv_create_ex(int pool_pages, int page_size, int heads, int head_dim, int layers,
+                         int max_streams, pkv_t* out) {
+  if (!out) return fail(nullptr, PKV_ERR_INVALID, "null output handle");
+  *out = nullptr;
+  if (head_dim != kHeadDim) return fail(nullptr, PKV_ERR_INVALID, "head_dim must be 64");
+  if (page_size < 16 || page_size > 256 || page_size % 16 != 0 ||
+      !(64 % page_size == 0 || page_size % 64 == 0))
+    return fail(nullptr, PKV_ERR_INVALID,
+                "page_size must be a multiple of 16 in [16, 256] dividing or divisible by 64");
+  if (pool_pages < 1 || heads < 1 || heads > 32 || layers < 1 || max_streams < 1 ||
+      max_streams > 1024)
+    return fail(nullptr, PKV_ERR_INVALID, "bad pool/heads/layers/max_streams");
+  pkv_t h = new pkv_ctx();
+  h->P = pool_pages;
+  h->Ps = page_size;
+  h->H = heads;
+  h->D = head_dim;
+  h->L = layers;
+  h->max_streams = max_streams;
+  h->page_elems = 2LL * heads * page_size * head_dim;
+  h->streams.resize(max_streams);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  const size_t pool_bytes = (size_t)layers * pool_pages * h->page_elems * sizeof(uint16_t);
+  if (e == cudaSuccess) e = cudaMalloc(&h->d_pool, pool_bytes);
+  if (e == cudaSuccess) e = cudaMemset(h->d_pool, 0, pool_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->d_free, sizeof(int32_t) * pool_pages);
+  if (e == cudaSuccess) e = cudaMalloc(&h->d_err, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
+  if (e == cudaSuccess) {
+    // free stack bottom..top = P-1 .. 0, so pops hand out 0, 1, 2, ...
+    std::vector<int32_t> init(pool_pages);
+    for (int i = 0; i < pool_pages; ++i) init[i] = pool_pages - 1 - i;
+    e = cudaMemcpy(h->d_free, init.data(), sizeof(int32_t) * pool_pages, cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) {
+    std::string msg = std::string("pkv_create: ") + cudaGetErrorString(e);
+    pkv_destroy(h);
+    return fail(nullptr, e == cudaErrorMemoryAllocation ? PKV_ERR_OOM : PKV_ERR_CUDA, "%s",
+                msg.c_str());
+  }
+  h->free_top = pool_pages;
+  *out = h;
+  return PKV_OK;
+}
+
+pkv_status pkv_destroy(pkv_t h) {
+  if (!h) return PKV_OK;
+  cudaDeviceSynchronize();
+  for (auto& st : h->streams)
+    if (st.d_mem) cudaFree(st.d_mem);
+  if (h->d_pool) cudaFree(h->d_pool);
+  if (h->d_free) cudaFree(h->d_free);
+  if (h->d_err) cudaFree(h->d_err);
+  if (h->d_scratch) cudaFree(h->d_scratch);
+  delete h;
+  return PKV_OK;
+}
+
+pkv_status pkv_stream_open(pkv_t h, const pkv_stream_cfg* cfg, int* stream_id) {
+  if (!h || !cfg || !stream_id) return fail(h, PKV_ERR_INVALID, "null argument");
+  const pkv_stream_cfg c = *cfg;
+  size_t words = 0;
+  Stream st;
+  st.cfg = c;
+  if (c.mode == PKV_MODE_FRAME) {
+    if (c.n_patch != h->Ps) return fail(h, PKV_ERR_INVALID, "n_patch must equal page_size");
+    if (c.n_special < 1 || c.n_special > h->Ps)
+      return fail(h, PKV_ERR_INVALID, "n_special must be in [1, page_size]");
+    if (c.num_scale < 0 || c.window < 1)
+      return fail(h, PKV_ERR_INVALID, "num_scale >= 0 and window >= 1 required");
+    if (c.window_slots < 0) return fail(h, PKV_ERR_INVALID, "window_slots must be >= 0");
+    if (c.window_slots > 0 &&
+        !(c.overlap_keyframes >= 0 && c.overlap_keyframes <= c.num_scale &&
+          c.overlap_keyframes < c.window_slots && c.overlap_keyframes <= kMaxCarry))
+      return fail(h, PKV_ERR_INVALID, "overlap_keyframes must be <= num_scale and < window_slots");
+    st.f_sp = h->Ps / c.n_special;
+    st.tbl_cap = c.num_scale + c.window + h->P;
+    words = (size_t)c.num_scale + c.window + h->P + 2 * (size_t)st.tbl_cap;
+  } else if (c.mode == PKV_MODE_CHUNKED) {
+    if (c.chunk_size < 1 || c.tokens_per_frame < 1 || c.sliding_window_num < 1 ||
+        c.sliding_window_num > kMaxChunks)
+      return fail(h, PKV_ERR_INVALID, "chunk_size, tokens_per_frame >= 1; sliding_window_num in [1,16]");
+    if ((long long)c.chunk_size * c.tokens_per_frame > (1LL << 24))
+      return fail(h, PKV_ERR_INVALID, "chunk too large");
+    if (ceil_div(c.tokens_per_frame, h->Ps) + 1 > 256)
+      return fail(h, PKV_ERR_INVALID, "a frame may not need more than 256 pages");
+    st.ppc = ceil_div((long long)c.chunk_size * c.tokens_per_frame, h->Ps);
+    st.tbl_cap = c.sliding_window_num * st.ppc;
+    words = (size_t)st.tbl_cap + 2 * (size_t)st.tbl_cap;
+  } else {
+    return fail(h, PKV_ERR_INVALID, "unknown mode %d", c.mode);
+  }
+  int sid = -1;
+  for (int i = 0; i < h->max_streams; ++i)
+    if (!h->streams[i].open) {
+      sid = i;
+      break;
+    }
+  if (sid < 0) return fail(h, PKV_ERR_OOM, "no free stream id");
+  cudaError_t e = cudaMalloc(&st.d_mem, words * sizeof(int32_t));
+  if (e != cudaSuccess) return cuda_fail(h, e, "stream_open cudaMalloc");
+  e = cudaMemset(st.d_mem, 0, words * sizeof(int32_t));
+  if (e != cudaSuccess) {
+    cudaFree(st.d_mem);
+    return cuda_fail(h, e, "stream_open cudaMemset");
+  }
+  int32_t* p = st.d_mem;
+  if (c.mode == PKV_MODE_FRAME) {
+    st.d_scale = p;
+    p += c.num_scale;
+    st.d_window = p;
+    p += c.window;
+    st.d_special = p;
+    p += h->P;
+  } else {
+    st.d_chunks = p;
+    p += st.tbl_cap;
+  }
+  st.d_tbl_idx = p;
+  p += st.tbl_cap;
+  st.d_tbl_len = p;
+  st.open = true;
+  h->streams[sid] = st;
+  *stream_id = sid;
+  return PKV_OK;
+}
+
+static pkv_status free_stream_pages(pkv_t h, Stream* st, cudaStream_t s) {
+  std::vector<PushSegment> segs;
+  if (st->cfg.mode == PKV_MODE_FRAME) {
+    segs.push_back(seg(st->d_scale, 0, st->n_scale));
+    segs.push_back(seg(st->d_window, st->win_head, st->win_count, 1, st->cfg.window));
+    segs.push_back(seg(st->d_special, 0, st->n_special));
+  } else {
+    for (int i = 0; i < st->n_chunks; ++i) {
+      const int slot = (st->c_head + i) % st->cfg.sliding_window_num;
+      segs.push_back(seg(st->d_chunks + (long long)slot * st->ppc, 0, st->c_pages[slot]));
+    }
+  }
+  return push_pages(h, segs.data(), (int)segs.size(), s);
+}
+
+static void clear_counters(Stream* st) {
+  Stream fresh;
+  fresh.open = true;
+  fresh.cfg = st->cfg;
+  fresh.d_mem = st->d_mem;
+  fresh.d_scale = st->d_scale;
+  fresh.d_window = st->d_window;
+  fresh.d_special = st->d_special;
+  fresh.d_chunks = st->d_chunks;
+  fresh.d_tbl_idx = st->d_tbl_idx;
+  fresh.d_tbl_len = st->d_tbl_len;
+  fresh.tbl_cap = st->tbl_cap;
+  fresh.f_sp = st->f_sp;
+  fresh.ppc = st->ppc;
+  *st = fresh;
+}
+
+pkv_status pkv_stream_close(pkv_t h, int sid, void* cuda_stream) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  if (pkv_status r = free_stream_pages(h, st, as_stream(cuda_stream))) return r;
+  // the list memory may still be read by the push just launched
+  PKV_CUDA(h, cudaStreamSynchronize(as_stream(cuda_stream)));
+  cudaFree(st->d_mem);
+  *st = Stream();
+  return PKV_OK;
+}
+
+pkv_status pkv_stream_reset(pkv_t h, int sid, void* cuda_stream) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  if (pkv_status r = free_stream_pages(h, st, as_stream(cuda_stream))) return r;
+  clear_counters(st);
+  return PKV_OK;
+}
+
+static pkv_status append_chunked(pkv_t h, Stream* st, int layer, const void* k, const void* v,
+                                 int n_tokens, cudaStream_t s) {
+  const int Wc = st->cfg.sliding_window_num;
+  ChunkAppendArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.pool = pool_view(h, layer);
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.n_tokens = n_tokens;
+  a.free_stack = h->d_free;
+  a.err = h->d_err;
+  if (layer == 0) {
+    const bool new_chunk = !st->c_open;
+    const int cur = (st->c_head + st->n_chunks - 1 + Wc) % Wc;
+    if (new_chunk && st->n_chunks == Wc)
+      return fail(h, PKV_ERR_STATE, "window holds sliding_window_num chunks: evict first");
+    if (!new_chunk && st->c_frames[cur] == st->cfg.chunk_size)
+      return fail(h, PKV_ERR_STATE, "chunk is full: evict before the next chunk");
+    const int slot = new_chunk ? (st->c_head + st->n_chunks) % Wc : cur;
+    const int len = new_chunk ? 0 : st->c_len[slot];
+    const int have = new_chunk ? 0 : st->c_pages[slot];
+    const int need = ceil_div(len + n_tokens, h->Ps) - have;
+    if (need > h->free_top) return fail(h, PKV_ERR_OOM, "free list exhausted (%d pages needed, %d free)", need, h->free_top);
+    a.top = h->free_top;
+    a.is_meta = 1;
+    a.chunk_pages = st->d_chunks + (long long)slot * st->ppc;
+    a.old_pages = have;
+    a.n_new = need;
+    a.pos0 = len;
+    PKV_CUDA(h, launch_chunk_append(a, s));
+    h->free_top -= need;
+    if (new_chunk) {
+      st->n_chunks++;
+      st->c_open = true;
+      st->c_len[slot] = st->c_pages[slot] = st->c_frames[slot] = 0;
+    }
+    st->c_pages[slot] += need;
+    st->c_len[slot] += n_tokens;
+    st->c_frames[slot] += 1;
+    st->pending = true;
+    st->u_new_chunk = new_chunk;
+    st->u_n_new = need;
+    st->u_old_pages = have;
+    st->u_pos0 = len;
+    st->u_slot = slot;
+  } else {
+    if (!st->pending) return fail(h, PKV_ERR_STATE, "layer > 0 append without a pending frame");
+    a.top = h->free_top;
+    a.is_meta = 0;
+    a.chunk_pages = st->d_chunks + (long long)st->u_slot * st->ppc;
+    a.old_pages = st->u_old_pages;
+    a.n_new = st->u_n_new;
+    a.pos0 = st->u_pos0;
+    PKV_CUDA(h, launch_chunk_append(a, s));
+  }
+  return PKV_OK;
+}
+
+// Plan one frame-mode layer-0 append: fills the batch item, returns pages needed.
+static pkv_status plan_frame_append(pkv_t h, Stream* st, const void* k, const void* v,
+                                    AppendItem* it, int* need) {
+  const pkv_stream_cfg& c = st->cfg;
+  const bool to_scale = st->n_scale < c.num_scale;
+  if (!to_scale && st->win_count == c.window)
+    return fail(h, PKV_ERR_STATE, "window is full: evict before appending");
+  const bool new_sp = st->n_special == 0 || st->sp_len + c.n_special > st->f_sp * c.n_special;
+  it->k = static_cast<const uint16_t*>(k);
+  it->v = static_cast<const uint16_t*>(v);
+  it->patch_slot = to_scale ? st->d_scale + st->n_scale
+                            : st->d_window + (st->win_head + st->win_count) % c.window;
+  it->special_list = st->d_special;
+  it->sp_idx = new_sp ? st->n_special : st->n_special - 1;
+  it->sp_off = new_sp ? 0 : st->sp_len;
+  it->new_sp = new_sp ? 1 : 0;
+  it->pad_ = 0;
+  *need = 1 + (new_sp ? 1 : 0);
+  return PKV_OK;
+}
+
+static void commit_frame_append(pkv_t h, Stream* st, const AppendItem& it) {
+  const pkv_stream_cfg& c = st->cfg;
+  const bool to_scale = st->n_scale < c.num_scale;
+  st->u_to_scale = to_scale;
+  st->u_new_sp = it.new_sp != 0;
+  st->u_sp_before = st->sp_len;
+  st->u_sp_off = it.sp_off;
+  if (to_scale) {
+    st->u_patch_pos = st->n_scale;
+    st->n_scale++;
+  } else {
+    st->u_patch_pos = (st->win_head + st->win_count) % c.window;
+    st->win_count++;
+  }
+  if (it.new_sp) {
+    st->n_special++;
+    st->sp_len = 0;
+  }
+  st->sp_len += c.n_special;
+  st->kept++;
+  st->pending = true;
+  h->free_top -= 1 + it.new_sp;
+}
+
+static void pending_item(Stream* st, const void* k, const void* v, AppendItem* it) {
+  it->k = static_cast<const uint16_t*>(k);
+  it->v = static_cast<const uint16_t*>(v);
+  it->patch_slot = (st->u_to_scale ? st->d_scale : st->d_window) + st->u_patch_pos;
+  it->special_list = st->d_special;
+  it->sp_idx = st->n_special - 1;
+  it->sp_off = st->u_sp_off;
+  it->new_sp = st->u_new_sp ? 1 : 0;
+  it->pad_ = 0;
+}
+
+pkv_status pkv_append_frames(pkv_t h, int n, const int* sids, int layer, const void* const* k,
+                             const void* const* v, int n_tokens, void* cuda_stream) {
+  if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
+  if (n < 1 || n > kMaxBatch || !sids || !k || !v)
+    return fail(h, PKV_ERR_INVALID, "batch of 1..32 streams with k and v arrays required");
+  if (layer < 0 || layer >= h->L) return fail(h, PKV_ERR_INVALID, "layer %d out of range", layer);
+  FrameAppendArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.pool = pool_view(h, layer);
+  a.free_stack = h->d_free;
+  a.top = h->free_top;
+  a.is_meta = layer == 0 ? 1 : 0;
+  a.n = n;
+  a.err = h->d_err;
+  int total_need = 0;
+  Stream* sts[kMaxBatch];
+  for (int i = 0; i < n; ++i) {
+    Stream* st = nullptr;
+    if (pkv_status r = get_stream(h, sids[i], &st)) return r;
+    for (int j = 0; j < i; ++j)
+      if (sids[j] == sids[i]) return fail(h, PKV_ERR_INVALID, "stream %d twice in one batch", sids[i]);
+    if (st->cfg.mode != PKV_MODE_FRAME)
+      return fail(h, PKV_ERR_STATE, "stream %d is not a frame-mode stream", sids[i]);
+    if (n_tokens != st->cfg.n_patch + st->cfg.n_special)
+      return fail(h, PKV_ERR_INVALID, "n_tokens %d != n_patch + n_special", n_tokens);
+    if (!k[i] || !v[i] || !aligned16(k[i]) || !aligned16(v[i]))
+      return fail(h, PKV_ERR_INVALID, "k/v must be 16-byte aligned device pointers");
+    if (i > 0 && st->cfg.n_special != sts[0]->cfg.n_special)
+      return fail(h, PKV_ERR_INVALID, "a batch must share n_special");
+    sts[i] = st;
+    if (layer == 0) {
+      int need = 0;
+      if (pkv_status r = plan_frame_append(h, st, k[i], v[i], &a.item[i], &need)) return r;
+      total_need += need;
+    } else {
+      if (!st->pending) return fail(h, PKV_ERR_STATE, "layer > 0 append without a pending frame");
+      pending_item(st, k[i], v[i], &a.item[i]);
+    }
+  }
+  if (layer == 0 && total_need > h->free_top)
+    return fail(h, PKV_ERR_OOM, "free list exhausted (%d pages needed, %d free)", total_need,
+                h->free_top);
+  a.n_patch = sts[0]->cfg.n_patch;
+  a.n_special = sts[0]->cfg.n_special;
+  PKV_CUDA(h, launch_frame_append(a, as_stream(cuda_stream)));
+  if (layer == 0)
+    for (int i = 0; i < n; ++i) commit_frame_append(h, sts[i], a.item[i]);
+  return PKV_OK;
+}
+
+pkv_status pkv_append_frame(pkv_t h, int sid, int layer, const void* k, const void* v,
+                            int n_tokens, void* cuda_stream) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  if (layer < 0 || layer >= h->L) return fail(h, PKV_ERR_INVALID, "layer %d out of range", layer);
+  if (!k || !v || !aligned16(k) || !aligned16(v))
+    return fail(h, PKV_ERR_INVALID, "k/v must be 16-byte aligned device pointers");
+  if (st->cfg.mode == PKV_MODE_CHUNKED) {
+    if (n_tokens != st->cfg.tokens_per_frame)
+      return fail(h, PKV_ERR_INVALID, "n_tokens %d != tokens_per_frame", n_tokens);
+    return append_chunked(h, st, layer, k, v, n_tokens, as_stream(cuda_stream));
+  }
+  const void* ks[1] = {k};
+  const void* vs[1] = {v};
+  return pkv_append_frames(h, 1, &sid, layer, ks, vs, n_tokens, cuda_stream);
+}
+
+pkv_status pkv_rollback_last_frame(pkv_t h, int sid, void* cuda_stream) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  if (!st->pending) return fail(h, PKV_ERR_STATE, "nothing to roll back");
+  cudaStream_t s = as_stream(cuda_stream);
+  if (st->cfg.mode == PKV_MODE_CHUNKED) {
+    const int slot = st->u_slot;
+    PushSegment g = seg(st->d_chunks + (long long)slot * st->ppc, st->u_old_pages + st->u_n_new - 1,
+                        st->u_n_new, -1);
+    if (pkv_status r = push_pages(h, &g, 1, s)) return r;
+    st->c_pages[slot] -= st->u_n_new;
+    st->c_len[slot] -= st->cfg.tokens_per_frame;
+    st->c_frames[slot] -= 1;
+    if (st->u_new_chunk) {
+      st->n_chunks--;
+      st->c_open = false;
+    }
+    st->pending = false;
+    return PKV_OK;
+  }
+  // special page first (popped last), then the patch page: the LIFO inverse
+  PushSegment segs[2];
+  int ns = 0;
+  if (st->u_new_sp) segs[ns++] = seg(st->d_special, st->n_special - 1, 1);
+  segs[ns++] = seg(st->u_to_scale ? st->d_scale : st->d_window, st->u_patch_pos, 1);
+  if (pkv_status r = push_pages(h, segs, ns, s)) return r;
+  if (st->u_new_sp) st->n_special--;
+  st->sp_len = st->u_sp_before;
+  if (st->u_to_scale) st->n_scale--;
+  else st->win_count--;
+  st->kept--;
+  st->pending = false;
+  return PKV_OK;
+}
+
+static pkv_status window_reset(pkv_t h, Stream* st, cudaStream_t s) {
+  const pkv_stream_cfg& c = st->cfg;
+  const int n_held = st->n_scale + st->win_count;
+  const int n_carry = std::min(c.overlap_keyframes, n_held);
+  const int n_new = ceil_div(n_carry, st->f_sp);
+  ResetCopyArgs ca;
+  std::memset(&ca, 0, sizeof(ca));
+  ca.pool = h->d_pool;
+  ca.layer_elems = (long long)h->P * h->page_elems;
+  ca.page_elems = h->page_elems;
+  ca.layers = h->L;
+  ca.heads = h->H;
+  ca.page_size = h->Ps;
+  ca.pool_pages = h->P;
+  ca.n_special = c.n_special;
+  ca.f_sp = st->f_sp;
+  ca.special_list = st->d_special;
+  ca.free_stack = h->d_free;
+  ca.top = h->free_top;
+  ca.n_carry = n_carry;
+  ca.n_new = n_new;
+  ca.err = h->d_err;
+  for (int i = 0; i < n_carry; ++i) {
+    const int j = n_held - n_carry + i;   // held position
+    const int kept_idx = j < st->n_scale ? j : st->kept - st->win_count + (j - st->n_scale);
+    ca.src_sp_idx[i] = kept_idx / st->f_sp;
+    ca.src_sp_off[i] = (kept_idx % st->f_sp) * c.n_special;
+  }
+  PKV_CUDA(h, launch_reset_copy(ca, s));
+  ResetMetaArgs ma;
+  std::memset(&ma, 0, sizeof(ma));
+  ma.free_stack = h->d_free;
+  ma.top = h->free_top;
+  ma.scale = st->d_scale;
+  ma.n_scale = st->n_scale;
+  ma.window = st->d_window;
+  ma.win_head = st->win_head;
+  ma.win_count = st->win_count;
+  ma.win_cap = c.window;
+  ma.special = st->d_special;
+  ma.n_special_old = st->n_special;
+  ma.n_carry = n_carry;
+  ma.n_new = n_new;
+  ma.pool_pages = h->P;
+  ma.err = h->d_err;
+  PKV_CUDA(h, launch_reset_meta(ma, s));
+  h->free_top += -n_new + (n_held - n_carry) + st->n_special;
+  st->n_scale = n_carry;
+  st->win_head = 0;
+  st->win_count = 0;
+  st->n_special = n_new;
+  st->sp_len = n_new ? (n_carry - (n_new - 1) * st->f_sp) * c.n_special : 0;
+  st->kept = n_carry;
+  return PKV_OK;
+}
+
+pkv_status pkv_evict_window(pkv_t h, int sid, void* cuda_stream) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  cudaStream_t s = as_stream(cuda_stream);
+  const pkv_stream_cfg& c = st->cfg;
+  if (c.mode == PKV_MODE_CHUNKED) {
+    const int Wc = c.sliding_window_num;
+    std::vector<PushSegment> segs;
+    int n_drop = std::max(0, st->n_chunks - (Wc - 1));
+    for (int i = 0; i < n_drop; ++i) {
+      const int slot = (st->c_head + i) % Wc;
+      segs.push_back(seg(st->d_chunks + (long long)slot * st->ppc, 0, st->c_pages[slot]));
+    }
+    if (pkv_status r = push_pages(h, segs.data(), (int)segs.size(), s)) return r;
+    st->c_head = (st->c_head + n_drop) % Wc;
+    st->n_chunks -= n_drop;
+    st->c_open = false;
+    st->pending = false;
+    return PKV_OK;
+  }
+  const int n_evict = std::max(0, st->win_count - (c.window - 1));
+  const bool reset = c.window_slots > 0 && st->kept >= c.window_slots;
+  if (reset) {
+    const int held = st->n_scale + st->win_count - n_evict;
+    const int n_new = ceil_div(std::min(c.overlap_keyframes, held), st->f_sp);
+    if (h->free_top + n_evict < n_new)
+      return fail(h, PKV_ERR_OOM, "free list exhausted by the window reset");
+    if (st->n_scale + st->win_count + st->n_special + n_new > 12 * 1024)
+      return fail(h, PKV_ERR_INVALID, "stream too large for a window reset");
+  }
+  if (n_evict > 0) {
+    PushSegment g = seg(st->d_window, st->win_head, n_evict, 1, c.window);
+    if (pkv_status r = push_pages(h, &g, 1, s)) return r;
+    st->win_head = (st->win_head + n_evict) % c.window;
+    st->win_count -= n_evict;
+  }
+  st->pending = false;
+  if (reset) return window_reset(h, st, s);
+  return PKV_OK;
+}
+
+pkv_status pkv_build_visible_page_table(pkv_t h, int sid, int32_t* d_idx, int32_t* d_len,
+                                        int capacity, int32_t* d_n, int32_t* d_last_page_len,
+                                        void* cuda_stream) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  int np, nt, last;
+  visible_counts(h, *st, &np, &nt, &last);
+  if (np > 0 && (!d_idx || !d_len)) return fail(h, PKV_ERR_INVALID, "null table buffers");
+  if (capacity < np) return fail(h, PKV_ERR_INVALID, "capacity %d < %d entries", capacity, np);
+  TableArgs t = table_args(h, *st, d_idx, d_len, d_n, d_last_page_len);
+  PKV_CUDA(h, launch_table(t, as_stream(cuda_stream)));
+  return PKV_OK;
+}
+
+static pkv_status ensure_scratch(pkv_t h, size_t bytes) {
+  if (bytes <= h->scratch_bytes) return PKV_OK;
+  PKV_CUDA(h, cudaDeviceSynchronize());
+  if (h->d_scratch) cudaFree(h->d_scratch);
+  h->d_scratch = nullptr;
+  h->scratch_bytes = 0;
+  PKV_CUDA(h, cudaMalloc(&h->d_scratch, bytes));
+  h->scratch_bytes = bytes;
+  return PKV_OK;
+}
+
+static pkv_status attend_common(pkv_t h, Stream* st, const void* q, int n_q, int layer, void* out,
+                                float sm_scale, cudaStream_t s) {
+  if (!q || !out || !aligned16(q) || !aligned16(out))
+    return fail(h, PKV_ERR_INVALID, "q/out must be 16-byte aligned device pointers");
+  if (n_q < 1 || n_q > (1 << 20)) return fail(h, PKV_ERR_INVALID, "n_q %d out of range", n_q);
+  if (layer < 0 || layer >= h->L) return fail(h, PKV_ERR_INVALID, "layer %d out of range", layer);
+  int np, nt, last;
+  visible_counts(h, *st, &np, &nt, &last);
+  if (nt == 0) return fail(h, PKV_ERR_STATE, "nothing is visible");
+  TableArgs t = table_args(h, *st, st->d_tbl_idx, st->d_tbl_len, nullptr, nullptr);
+  PKV_CUDA(h, launch_table(t, s));
+  AttendArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = static_cast<const uint16_t*>(q);
+  a.out = static_cast<uint16_t*>(out);
+  a.n_q = n_q;
+  a.heads = h->H;
+  a.pool = h->d_pool + (long long)layer * h->P * h->page_elems;
+  a.page_elems = h->page_elems;
+  a.page_size = h->Ps;
+  a.pool_pages = h->P;
+  a.tbl_idx = st->d_tbl_idx;
+  a.tbl_len = st->d_tbl_len;
+  a.n_entries = np;
+  a.n_tiles = ceil_div((long long)(np - 1) * h->Ps + last, 64);
+  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)h->D);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.num_splits = attend_num_splits(n_q, h->H, a.n_tiles, h->num_sms);
+  a.err = h->d_err;
+  if (a.num_splits > 1) {
+    const size_t o_bytes = (size_t)a.num_splits * n_q * h->H * kHeadDim * sizeof(float);
+    const size_t ml_bytes = (size_t)a.num_splits * n_q * h->H * 2 * sizeof(float);
+    if (pkv_status r = ensure_scratch(h, o_bytes + ml_bytes)) return r;
+    a.part_o = h->d_scratch;
+    a.part_ml = h->d_scratch + o_bytes / sizeof(float);
+  }
+  PKV_CUDA(h, launch_attend(a, h->num_sms, s));
+  return PKV_OK;
+}
+
+pkv_status pkv_attend(pkv_t h, const void* q, int n_q, int sid, int layer, void* out,
+                      float sm_scale, void* cuda_stream) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  if (st->cfg.mode != PKV_MODE_FRAME)
+    return fail(h, PKV_ERR_STATE, "pkv_attend needs a frame-mode stream (use pkv_attend_chunked)");
+  return attend_common(h, st, q, n_q, layer, out, sm_scale, as_stream(cuda_stream));
+}
+
+pkv_status pkv_attend_chunked(pkv_t h, const void* q, int n_q, int sid, int layer, void* out,
+                              float sm_scale, void* cuda_stream) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  if (st->cfg.mode != PKV_MODE_CHUNKED)
+    return fail(h, PKV_ERR_STATE, "pkv_attend_chunked needs a chunked-mode stream");
+  if (!st->c_open) return fail(h, PKV_ERR_STATE, "no open chunk");
+  const int cur = (st->c_head + st->n_chunks - 1) % st->cfg.sliding_window_num;
+  if (n_q != st->c_len[cur])
+    return fail(h, PKV_ERR_INVALID, "n_q %d != the open chunk's %d tokens", n_q, st->c_len[cur]);
+  return attend_common(h, st, q, n_q, layer, out, sm_scale, as_stream(cuda_stream));
+}
+
+pkv_status pkv_sync(pkv_t h, void* cuda_stream) {
+  if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
+  PKV_CUDA(h, cudaStreamSynchronize(as_stream(cuda_stream)));
+  PKV_CUDA(h, cudaGetLastError());
+  int err = 0;
+  PKV_CUDA(h, cudaMemcpy(&err, h->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (err & kErrTimeout) return fail(h, PKV_ERR_TIMEOUT, "a bounded device wait gave up (0x%x)", err);
+  if (err) return fail(h, PKV_ERR_DEVICE, "device error word 0x%x (page id outside the pool)", err);
+  return PKV_OK;
+}
+
+pkv_status pkv_visible_count(pkv_t h, int sid, int* n_pages, int* n_tokens) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  int np, nt, last;
+  visible_counts(h, *st, &np, &nt, &last);
+  if (n_pages) *n_pages = np;
+  if (n_tokens) *n_tokens = nt;
+  return PKV_OK;
+}
+
+pkv_status pkv_free_pages(pkv_t h, int* n_free) {
+  if (!h || !n_free) return fail(h, PKV_ERR_INVALID, "null argument");
+  *n_free = h->free_top;
+  return PKV_OK;
+}
+
+pkv_status pkv_export_state(pkv_t h, int sid, int32_t* host_buf, size_t cap_words,
+                            size_t* used_words) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  if (!host_buf || !used_words) return fail(h, PKV_ERR_INVALID, "null argument");
+  int np, nt, last;
+  visible_counts(h, *st, &np, &nt, &last);
+  const size_t need = 1 + (size_t)h->free_top + 1 + 2 * (size_t)np + 6 + 3 + kMaxChunks;
+  if (cap_words < need) return fail(h, PKV_ERR_INVALID, "export needs %zu words", need);
+  PKV_CUDA(h, cudaDeviceSynchronize());
+  std::vector<int32_t> buf;
+  buf.push_back(h->free_top);
+  std::vector<int32_t> fs(h->free_top);
+  if (h->free_top)
+    PKV_CUDA(h, cudaMemcpy(fs.data(), h->d_free, sizeof(int32_t) * h->free_top, cudaMemcpyDeviceToHost));
+  buf.insert(buf.end(), fs.begin(), fs.end());
+  buf.push_back(np);
+  if (np) {
+    TableArgs t = table_args(h, *st, st->d_tbl_idx, st->d_tbl_len, nullptr, nullptr);
+    PKV_CUDA(h, launch_table(t, 0));
+    PKV_CUDA(h, cudaDeviceSynchronize());
+    std::vector<int32_t> idx(np), len(np);
+    PKV_CUDA(h, cudaMemcpy(idx.data(), st->d_tbl_idx, sizeof(int32_t) * np, cudaMemcpyDeviceToHost));
+    PKV_CUDA(h, cudaMemcpy(len.data(), st->d_tbl_len, sizeof(int32_t) * np, cudaMemcpyDeviceToHost));
+    buf.insert(buf.end(), idx.begin(), idx.end());
+    buf.insert(buf.end(), len.begin(), len.end());
+  }
+  if (st->cfg.mode == PKV_MODE_FRAME) {
+    int32_t w[6] = {st->n_scale, st->win_count, st->n_special, st->sp_len, st->kept, st->pending};
+    buf.insert(buf.end(), w, w + 6);
+  } else {
+    buf.push_back(st->n_chunks);
+    buf.push_back(st->c_open);
+    buf.push_back(st->pending);
+    for (int i = 0; i < st->n_chunks; ++i)
+      buf.push_back(st->c_len[(st->c_head + i) % st->cfg.sliding_window_num]);
+  }
+  std::memcpy(host_buf, buf.data(), buf.size() * sizeof(int32_t));
+  *used_words = buf.size();
+  return PKV_OK;
+}
+
+pkv_status pkv_read_page(pkv_t h, int layer, int page, int kv, void* host_dst) {
+  if (!h || !host_dst) return fail(h, PKV_ERR_INVALID, "null argument");
+  if (layer < 0 || layer >= h->L || page < 0 || page >= h->P || (kv != 0 && kv != 1))
+    return fail(h, PKV_ERR_INVALID, "layer/page/kv out of range");
+  const size_t n = (size_t)h->H * h->Ps * kHeadDim;
+  std::vector<uint16_t> raw(n);
+  PKV_CUDA(h, cudaDeviceSynchronize());
+  const uint16_t* src = h->d_pool + (long long)layer * h->P * h->page_elems +
+                        (long long)page * h->page_elems + (long long)kv * n;
+  PKV_CUDA(h, cudaMemcpy(raw.data(), src, n * sizeof(uint16_t), cudaMemcpyDeviceToHost));
+  uint16_t* dst = static_cast<uint16_t*>(host_dst);
+  for (int hh = 0; hh < h->H; ++hh)
+    for (int s = 0; s < h->Ps; ++s)
+      for (int c = 0; c < kChunksPerRow; ++c) {
+        const size_t row = ((size_t)hh * h->Ps + s) * kHeadDim;
+        std::memcpy(dst + row + c * 8, raw.data() + row + swizzle_chunk(s, c) * 8, 16);
+      }
+  return PKV_OK;
+}
+
+pkv_status pkv_synth_fill(void* dst, int n_frames, int n_tokens, int heads, int head_dim,
+                          int seed, int workload, int stream, int layer, int frame0, int tensor,
+                          int token0, float scale, void* cuda_stream) {
+  if (!dst || n_frames < 0 || n_tokens < 0 || heads < 1 || heads > 32 || head_dim < 1 ||
+      head_dim > 64 || seed < 0 || seed >= 128 || workload < 0 || workload >= 8 || stream < 0 ||
+      stream >= 64 || layer < 0 || layer >= 32 || frame0 < 0 || frame0 + n_frames > 65536 ||
+      tensor < 0 || tensor >= 4 || token0 < 0 || token0 + n_tokens > 16384)
+    return fail(nullptr, PKV_ERR_INVALID, "pkv_synth_fill: argument out of range");
+  int e2;
+  const float m = std::frexp(scale, &e2);
+  if (m != 0.5f) return fail(nullptr, PKV_ERR_INVALID, "pkv_synth_fill: scale must be a power of two");
+  const unsigned long long key_base =
+      ((unsigned long long)seed << 57) | ((unsigned long long)workload << 54) |
+      ((unsigned long long)stream << 48) | ((unsigned long long)layer << 43) |
+      ((unsigned long long)tensor << 25);
+  cudaError_t e = launch_synth(static_cast<uint16_t*>(dst), n_frames, n_tokens, heads, head_dim,
+                               key_base, frame0, token0, scale, as_stream(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "pkv_synth_fill");
+  return PKV_OK;
+}
+
+}  // extern "C"

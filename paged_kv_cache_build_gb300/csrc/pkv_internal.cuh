@@ -1,0 +1,191 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+constexpr int kHeadDim = 64;        // bf16 elements per (slot, head) row: 128 bytes
+constexpr int kChunksPerRow = 8;    // 16-byte chunks per row
+constexpr int kMaxBatch = 32;       // streams per batched append
+constexpr int kMaxChunks = 16;      // chunks visible at once (chunked mode)
+constexpr int kMaxSegments = 20;    // page-id segments one push launch can return
+constexpr int kMaxCarry = 64;       // overlap keyframes carried by a window reset
+
+// Bits of the device error word.
+enum : int {
+  kErrPageRange = 1,   // a page id outside [0, pool_pages) was read from the metadata
+  kErrTimeout = 2,     // a bounded wait gave up
+};
+
+// 128-byte-swizzled storage: logical 16-byte chunk c of slot s sits at c ^ (s & 7).
+__host__ __device__ __forceinline__ int swizzle_chunk(int slot, int chunk) {
+  return chunk ^ (slot & 7);
+}
+
+// One layer's page set: pool[page][kv][head][slot][64].
+struct PoolView {
+  uint16_t* base;
+  long long page_elems;   // 2 * heads * page_size * 64
+  int heads;
+  int page_size;
+  int pool_pages;
+};
+
+// ------------------------------------------------------------------ append
+struct AppendItem {                 // one frame-mode stream of a batched append
+  const uint16_t* k;
+  const uint16_t* v;
+  int32_t* patch_slot;              // list entry that receives / holds the patch page id
+  int32_t* special_list;            // the stream's special page list
+  int sp_idx;                       // list index of the special page this frame writes
+  int sp_off;                       // first special slot this frame writes
+  int new_sp;                       // this frame opened special_list[sp_idx]
+  int pad_;
+};
+
+struct FrameAppendArgs {
+  PoolView pool;
+  int n_patch;
+  int n_special;
+  int32_t* free_stack;
+  int top;                          // free-stack depth before this batch's pops
+  int is_meta;                      // pop pages and write the lists (first layer of the frame)
+  int n;                            // streams in the batch
+  int* err;
+  AppendItem item[kMaxBatch];
+};
+
+struct ChunkAppendArgs {
+  PoolView pool;
+  const uint16_t* k;
+  const uint16_t* v;
+  int n_tokens;
+  int32_t* free_stack;
+  int top;
+  int is_meta;
+  int32_t* chunk_pages;             // the open chunk's page list
+  int old_pages;                    // pages the chunk held before this append
+  int n_new;                        // pages this append pops
+  int pos0;                         // tokens the chunk held before this append
+  int* err;
+};
+
+// ------------------------------------------------------------ push (free)
+struct PushSegment {                // page ids src[(start + step*j) mod ring], j < count
+  const int32_t* src;
+  int start;
+  int count;
+  int step;                         // +1 or -1
+  int ring;                         // 0: linear
+};
+
+struct PushArgs {
+  int32_t* free_stack;
+  int top;                          // depth before the pushes
+  int n_seg;
+  int pool_pages;
+  int* err;
+  PushSegment seg[kMaxSegments];
+};
+
+// ----------------------------------------------------------- window reset
+struct ResetCopyArgs {              // copy carried frames' special tokens, all layers
+  uint16_t* pool;                   // layer 0 base
+  long long layer_elems;            // pool_pages * page_elems
+  long long page_elems;
+  int layers, heads, page_size, pool_pages;
+  int n_special, f_sp;
+  const int32_t* special_list;      // old special list
+  const int32_t* free_stack;
+  int top;                          // depth after the eviction, before the reset's pops
+  int n_carry;
+  int src_sp_idx[kMaxCarry];        // special list index of carried frame i
+  int src_sp_off[kMaxCarry];        // its first slot there
+  int n_new;                        // special pages the reset pops
+  int* err;
+};
+
+struct ResetMetaArgs {
+  int32_t* free_stack;
+  int top;                          // depth after the eviction, before the reset's pops
+  int32_t* scale;                   // scale list
+  int n_scale;
+  int32_t* window;                  // window ring
+  int win_head, win_count, win_cap;
+  int32_t* special;
+  int n_special_old;
+  int n_carry;                      // the last n_carry held pages are carried
+  int n_new;
+  int pool_pages;
+  int* err;
+};
+
+// ------------------------------------------------------------------ table
+struct TableArgs {
+  int mode;
+  int n;                            // entries
+  int page_size;
+  int pool_pages;
+  // frame mode
+  const int32_t* scale;
+  int n_scale;
+  const int32_t* window;
+  int win_head, win_count, win_cap;
+  const int32_t* special;
+  int n_special;
+  int sp_full_len;
+  int sp_last_len;
+  // chunked mode (oldest chunk first)
+  int n_chunks;
+  const int32_t* chunk_pages[kMaxChunks];
+  int chunk_npages[kMaxChunks];
+  int chunk_len[kMaxChunks];
+  // outputs
+  int32_t* out_idx;
+  int32_t* out_len;
+  int32_t* out_n;                   // may be null
+  int32_t* out_last;                // may be null
+  int* err;
+};
+
+// ---------------------------------------------------------------- attend
+struct AttendArgs {
+  const uint16_t* q;                // [n_q][heads][64]
+  uint16_t* out;                    // [n_q][heads][64] (written when num_splits == 1)
+  int n_q;
+  int heads;
+  const uint16_t* pool;             // layer base
+  long long page_elems;
+  int page_size;
+  int pool_pages;
+  const int32_t* tbl_idx;
+  const int32_t* tbl_len;
+  int n_entries;
+  int n_tiles;                      // 64-slot tiles covering the table's slots
+  float scale_log2;                 // sm_scale * log2(e)
+  int num_splits;
+  float* part_o;                    // [split][n_q][heads][64]
+  float* part_ml;                   // [split][n_q][heads][2]  (running max, sum), log2 domain
+  int* err;
+};
+
+// Kernel launches made by this library in this process (every launcher counts).
+unsigned long long launch_count();
+void count_launches(int n);
+
+// Launchers (each returns the launch's cudaError_t).
+cudaError_t launch_frame_append(const FrameAppendArgs& a, cudaStream_t s);
+cudaError_t launch_chunk_append(const ChunkAppendArgs& a, cudaStream_t s);
+cudaError_t launch_push(const PushArgs& a, cudaStream_t s);
+cudaError_t launch_reset_copy(const ResetCopyArgs& a, cudaStream_t s);
+cudaError_t launch_reset_meta(const ResetMetaArgs& a, cudaStream_t s);
+cudaError_t launch_table(const TableArgs& a, cudaStream_t s);
+cudaError_t launch_attend(const AttendArgs& a, int num_sms, cudaStream_t s);
+int attend_num_splits(int n_q, int heads, int n_tiles, int num_sms);
+cudaError_t launch_synth(uint16_t* dst, int n_frames, int n_tokens, int heads, int head_dim,
+                         unsigned long long key_base, int frame0, int token0, float scale,
+                         cudaStream_t s);
+
+}  // namespace pkv

@@ -1,0 +1,385 @@
+// Page-pool metadata and KV movement kernels: append/scatter (frame and chunked
+// mode), pushes onto the free stack (rollback, eviction, close), the windowed
+// reset, and the visible-page-table build.
+//
+// "LingBot-Map Paged KV Cache", section 2: pages come from a free list; a page
+// that leaves the sliding window returns to it at once; special tokens are
+// appended floor(page_size / n_special) frames to a page; the visible table is
+// scale -> window -> special. Section 3: a non-keyframe's append is undone.
+// Section 4: a window reset carries the last overlap keyframes over.
+// vLLM-Omni RFC "Reconstruction Engine", section 3.3: chunk append / evict.
+//
+// The device holds page ids only (the free stack's array and each stream's
+// lists). Every count and list position is mirrored on the host and passed in,
+// so no kernel ever reads a count that another kernel is changing.
+#include <atomic>
+
+#include "pkv_internal.cuh"
+
+namespace pkv {
+
+namespace {
+
+__device__ __forceinline__ bool page_ok(int p, int pool_pages) {
+  return p >= 0 && p < pool_pages;
+}
+
+__device__ __forceinline__ uint16_t* row_ptr(const PoolView& pv, int page, int kv, int head,
+                                             int slot) {
+  return pv.base + (long long)page * pv.page_elems +
+         ((long long)(kv * pv.heads + head) * pv.page_size + slot) * kHeadDim;
+}
+
+// One batched frame-mode append. blockIdx.y selects the stream; every block
+// recomputes that stream's place on the free stack with an exclusive warp scan
+// of the batch's page needs (1, or 2 when the frame opens a special page), so
+// stream i pops after streams 0..i-1 exactly as sequential appends would.
+__global__ void __launch_bounds__(256) frame_append_kernel(const FrameAppendArgs a) {
+  const int b = blockIdx.y;
+  __shared__ int s_patch, s_sp;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int need = lane < a.n ? 1 + a.item[lane].new_sp : 0;
+    int incl = need;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += y;
+    }
+    const int off = __shfl_sync(0xffffffffu, incl - need, b);
+    if (lane == 0) {
+      const AppendItem& it = a.item[b];
+      int patch, sp;
+      if (a.is_meta) {
+        patch = a.free_stack[a.top - 1 - off];
+        sp = it.new_sp ? a.free_stack[a.top - 2 - off] : it.special_list[it.sp_idx];
+      } else {
+        patch = *it.patch_slot;
+        sp = it.special_list[it.sp_idx];
+      }
+      const bool ok = page_ok(patch, a.pool.pool_pages) && page_ok(sp, a.pool.pool_pages);
+      if (!ok) {
+        atomicOr(a.err, kErrPageRange);
+        patch = -1;
+      } else if (a.is_meta && blockIdx.x == 0) {
+        *it.patch_slot = patch;
+        if (it.new_sp) it.special_list[it.sp_idx] = sp;
+      }
+      s_patch = patch;
+      s_sp = sp;
+    }
+  }
+  __syncthreads();
+  const int patch = s_patch, sp = s_sp;
+  if (patch < 0) return;
+
+  const AppendItem& it = a.item[b];
+  const int H = a.pool.heads;
+  const int n_tok = a.n_patch + a.n_special;
+  // A freshly opened special page gets its unused slots zeroed, so that every
+  // slot of a held page is a token or zero.
+  const int zero_slots = it.new_sp ? a.pool.page_size - a.n_special : 0;
+  const long long per_tok = 2LL * H * kChunksPerRow;
+  const long long total = (long long)(n_tok + zero_slots) * per_tok;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int c = (int)(i & 7);
+    long long r = i >> 3;
+    const int h = (int)(r % H);
+    r /= H;
+    const int kv = (int)(r & 1);
+    const int t = (int)(r >> 1);
+    uint4 val;
+    int page, slot;
+    if (t < n_tok) {
+      const uint16_t* src = (kv ? it.v : it.k) + ((long long)t * H + h) * kHeadDim + c * 8;
+      val = __ldg(reinterpret_cast<const uint4*>(src));
+      if (t < a.n_patch) {
+        page = patch;
+        slot = t;
+      } else {
+        page = sp;
+        slot = it.sp_off + (t - a.n_patch);
+      }
+    } else {
+      val = make_uint4(0u, 0u, 0u, 0u);
+      page = sp;
+      slot = a.n_special + (t - n_tok);
+    }
+    uint16_t* dst = row_ptr(a.pool, page, kv, h, slot) + swizzle_chunk(slot, c) * 8;
+    *reinterpret_cast<uint4*>(dst) = val;
+  }
+}
+
+// Chunked-mode append: the frame's tokens are packed after the chunk's pos0
+// tokens; pages of the chunk past old_pages are popped by this append.
+__global__ void __launch_bounds__(256) chunk_append_kernel(const ChunkAppendArgs a) {
+  const int Ps = a.pool.page_size;
+  if (a.is_meta && blockIdx.x == 0 && threadIdx.x < a.n_new) {
+    const int p = a.free_stack[a.top - 1 - threadIdx.x];
+    if (page_ok(p, a.pool.pool_pages)) a.chunk_pages[a.old_pages + threadIdx.x] = p;
+    else atomicOr(a.err, kErrPageRange);
+  }
+  const int end = a.pos0 + a.n_tokens;
+  const int last_pi = (end - 1) / Ps;
+  // zero the tail of a freshly popped last page
+  const int zero_slots = (last_pi >= a.old_pages && (end % Ps) != 0) ? Ps - (end % Ps) : 0;
+  const int H = a.pool.heads;
+  const long long per_tok = 2LL * H * kChunksPerRow;
+  const long long total = (long long)(a.n_tokens + zero_slots) * per_tok;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int c = (int)(i & 7);
+    long long r = i >> 3;
+    const int h = (int)(r % H);
+    r /= H;
+    const int kv = (int)(r & 1);
+    const int t = (int)(r >> 1);
+    const int pos = a.pos0 + t;
+    const int pi = pos / Ps;
+    const int slot = pos - pi * Ps;
+    const int page = (pi < a.old_pages || !a.is_meta)
+                         ? a.chunk_pages[pi]
+                         : a.free_stack[a.top - 1 - (pi - a.old_pages)];
+    if (!page_ok(page, a.pool.pool_pages)) {
+      atomicOr(a.err, kErrPageRange);
+      continue;
+    }
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (t < a.n_tokens) {
+      const uint16_t* src = (kv ? a.v : a.k) + ((long long)t * H + h) * kHeadDim + c * 8;
+      val = __ldg(reinterpret_cast<const uint4*>(src));
+    }
+    uint16_t* dst = row_ptr(a.pool, page, kv, h, slot) + swizzle_chunk(slot, c) * 8;
+    *reinterpret_cast<uint4*>(dst) = val;
+  }
+}
+
+// Push page ids onto the free stack: free[top + j] for j over the segments in
+// order. Sources are stream lists, never the free stack itself.
+__global__ void __launch_bounds__(256) push_kernel(const PushArgs a) {
+  int total = 0;
+  for (int s = 0; s < a.n_seg; ++s) total += a.seg[s].count;
+  for (int j = threadIdx.x; j < total; j += blockDim.x) {
+    int s = 0, base = 0;
+    while (j >= base + a.seg[s].count) {
+      base += a.seg[s].count;
+      ++s;
+    }
+    const PushSegment& g = a.seg[s];
+    int pos = g.start + g.step * (j - base);
+    if (g.ring) pos = ((pos % g.ring) + g.ring) % g.ring;
+    const int p = g.src[pos];
+    if (!page_ok(p, a.pool_pages)) {
+      atomicOr(a.err, kErrPageRange);
+      continue;
+    }
+    a.free_stack[a.top + j] = p;
+  }
+}
+
+// Window reset, data part: copy each carried frame's special tokens (every
+// layer, K and V) into the freshly popped special pages free[top-1-k], and zero
+// those pages' unused slots.
+__global__ void __launch_bounds__(256) reset_copy_kernel(const ResetCopyArgs a) {
+  const int H = a.heads, Ps = a.page_size;
+  const long long per_slot = 2LL * H * kChunksPerRow;
+  const long long copy_total = (long long)a.layers * a.n_carry * a.n_special * per_slot;
+  const long long zero_total = (long long)a.layers * a.n_new * Ps * per_slot;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < copy_total + zero_total;
+       i += stride) {
+    const bool is_copy = i < copy_total;
+    long long r = is_copy ? i : i - copy_total;
+    const int c = (int)(r & 7);
+    r >>= 3;
+    const int h = (int)(r % H);
+    r /= H;
+    const int kv = (int)(r & 1);
+    r >>= 1;
+    int dst_page_k, dst_slot, layer;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (is_copy) {
+      const int j = (int)(r % a.n_special);
+      r /= a.n_special;
+      const int ci = (int)(r % a.n_carry);
+      layer = (int)(r / a.n_carry);
+      const int src_page = a.special_list[a.src_sp_idx[ci]];
+      if (!page_ok(src_page, a.pool_pages)) {
+        atomicOr(a.err, kErrPageRange);
+        continue;
+      }
+      const int src_slot = a.src_sp_off[ci] + j;
+      const uint16_t* src = a.pool + layer * a.layer_elems + (long long)src_page * a.page_elems +
+                            ((long long)(kv * H + h) * Ps + src_slot) * kHeadDim +
+                            swizzle_chunk(src_slot, c) * 8;
+      val = *reinterpret_cast<const uint4*>(src);
+      dst_page_k = ci / a.f_sp;
+      dst_slot = (ci % a.f_sp) * a.n_special + j;
+    } else {
+      const int slot = (int)(r % Ps);
+      r /= Ps;
+      dst_page_k = (int)(r % a.n_new);
+      layer = (int)(r / a.n_new);
+      const int frames_here = min(a.f_sp, a.n_carry - dst_page_k * a.f_sp);
+      if (slot < frames_here * a.n_special) continue;   // written by the copy part
+      dst_slot = slot;
+    }
+    const int dst_page = a.free_stack[a.top - 1 - dst_page_k];
+    if (!page_ok(dst_page, a.pool_pages)) {
+      atomicOr(a.err, kErrPageRange);
+      continue;
+    }
+    uint16_t* dst = a.pool + layer * a.layer_elems + (long long)dst_page * a.page_elems +
+                    ((long long)(kv * H + h) * Ps + dst_slot) * kHeadDim +
+                    swizzle_chunk(dst_slot, c) * 8;
+    *reinterpret_cast<uint4*>(dst) = val;
+  }
+}
+
+// Window reset, metadata part (one block): the last n_carry held pages become
+// the scale list, the popped pages the special list, and the other held pages
+// (scale, then window oldest first) and the old special pages are pushed.
+__global__ void __launch_bounds__(256) reset_meta_kernel(const ResetMetaArgs a) {
+  extern __shared__ int sm[];
+  const int n_held = a.n_scale + a.win_count;
+  int* held = sm;
+  int* old_sp = held + n_held;
+  int* new_sp = old_sp + a.n_special_old;
+  for (int j = threadIdx.x; j < n_held; j += blockDim.x)
+    held[j] = j < a.n_scale ? a.scale[j] : a.window[(a.win_head + j - a.n_scale) % a.win_cap];
+  for (int j = threadIdx.x; j < a.n_special_old; j += blockDim.x) old_sp[j] = a.special[j];
+  for (int k = threadIdx.x; k < a.n_new; k += blockDim.x) new_sp[k] = a.free_stack[a.top - 1 - k];
+  __syncthreads();
+  const int n_free_held = n_held - a.n_carry;
+  const int top2 = a.top - a.n_new;
+  for (int i = threadIdx.x; i < a.n_carry; i += blockDim.x) a.scale[i] = held[n_free_held + i];
+  for (int k = threadIdx.x; k < a.n_new; k += blockDim.x) a.special[k] = new_sp[k];
+  for (int j = threadIdx.x; j < n_free_held + a.n_special_old; j += blockDim.x) {
+    const int p = j < n_free_held ? held[j] : old_sp[j - n_free_held];
+    if (!page_ok(p, a.pool_pages)) {
+      atomicOr(a.err, kErrPageRange);
+      continue;
+    }
+    a.free_stack[top2 + j] = p;
+  }
+}
+
+// Visible page table: page ids and valid slot counts in attention order.
+__global__ void __launch_bounds__(256) table_kernel(const TableArgs a) {
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < a.n; e += gridDim.x * blockDim.x) {
+    int id, len;
+    if (a.mode == 0) {
+      if (e < a.n_scale) {
+        id = a.scale[e];
+        len = a.page_size;
+      } else if (e < a.n_scale + a.win_count) {
+        id = a.window[(a.win_head + e - a.n_scale) % a.win_cap];
+        len = a.page_size;
+      } else {
+        const int k = e - a.n_scale - a.win_count;
+        id = a.special[k];
+        len = (k == a.n_special - 1) ? a.sp_last_len : a.sp_full_len;
+      }
+    } else {
+      int c = 0, base = 0;
+      while (c < a.n_chunks - 1 && e >= base + a.chunk_npages[c]) {
+        base += a.chunk_npages[c];
+        ++c;
+      }
+      const int k = e - base;
+      id = a.chunk_pages[c][k];
+      len = min(a.page_size, a.chunk_len[c] - k * a.page_size);
+    }
+    if (!page_ok(id, a.pool_pages)) {
+      atomicOr(a.err, kErrPageRange);
+      id = 0;
+      len = 0;
+    }
+    a.out_idx[e] = id;
+    a.out_len[e] = len;
+  }
+}
+
+__global__ void table_tail_kernel(int32_t* out_n, int32_t* out_last, int n, int last) {
+  if (out_n) *out_n = n;
+  if (out_last) *out_last = last;
+}
+
+inline int blocks_for(long long work, int per_block, int cap) {
+  long long b = (work + per_block - 1) / per_block;
+  if (b < 1) b = 1;
+  if (b > cap) b = cap;
+  return (int)b;
+}
+
+}  // namespace
+
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+
+unsigned long long launch_count() { return g_launches.load(); }
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
+
+cudaError_t launch_frame_append(const FrameAppendArgs& a, cudaStream_t s) {
+  const long long per_stream = (long long)(a.n_patch + a.pool.page_size) * 2 * a.pool.heads * 8;
+  dim3 grid(blocks_for(per_stream, 256 * 4, 1024), a.n);
+  frame_append_kernel<<<grid, 256, 0, s>>>(a);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_append(const ChunkAppendArgs& a, cudaStream_t s) {
+  const long long work = (long long)(a.n_tokens + a.pool.page_size) * 2 * a.pool.heads * 8;
+  chunk_append_kernel<<<blocks_for(work, 256 * 4, 2048), 256, 0, s>>>(a);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_push(const PushArgs& a, cudaStream_t s) {
+  push_kernel<<<1, 256, 0, s>>>(a);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reset_copy(const ResetCopyArgs& a, cudaStream_t s) {
+  const long long work = (long long)a.layers * (a.n_carry * a.n_special + a.n_new * a.page_size) *
+                         2 * a.heads * 8;
+  if (work == 0) return cudaSuccess;
+  reset_copy_kernel<<<blocks_for(work, 256 * 4, 4096), 256, 0, s>>>(a);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reset_meta(const ResetMetaArgs& a, cudaStream_t s) {
+  const size_t smem = sizeof(int) * (size_t)(a.n_scale + a.win_count + a.n_special_old + a.n_new);
+  if (smem > 48 * 1024) return cudaErrorInvalidValue;
+  reset_meta_kernel<<<1, 256, smem, s>>>(a);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_table(const TableArgs& a, cudaStream_t s) {
+  if (a.n > 0) {
+    table_kernel<<<blocks_for(a.n, 256, 64), 256, 0, s>>>(a);
+    count_launches(1);
+  }
+  if (a.out_n || a.out_last) {
+    // the last entry's length is known on the host through the counts
+    int last = 0;
+    if (a.n > 0) {
+      if (a.mode == 0) {
+        last = a.n_special > 0 ? a.sp_last_len : a.page_size;
+      } else {
+        const int c = a.n_chunks - 1;
+        last = a.chunk_len[c] - (a.chunk_npages[c] - 1) * a.page_size;
+      }
+    }
+    table_tail_kernel<<<1, 1, 0, s>>>(a.out_n, a.out_last, a.n, last);
+    count_launches(1);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,57 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every entry point
+include/pkv.h declares (no compute calls: no GPU is needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = []
+    for f in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[\w\*\s]+?\b(pkv_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_build_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ("pkv_create", "pkv_append_frame", "pkv_rollback_last_frame", "pkv_evict_window",
+                     "pkv_build_visible_page_table", "pkv_attend", "pkv_attend_chunked"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_symbol(lib):
+    from paged_kv_cache_build_gb300._lib import SIGNATURES
+    assert set(declared_symbols()) <= set(SIGNATURES)
+
+
+def test_host_side_errors_without_gpu(lib):
+    """Argument checks run before any CUDA call."""
+    from paged_kv_cache_build_gb300._lib import load
+    L = load()
+    h = ctypes.c_void_p()
+    assert L.pkv_create(16, 256, 16, 128, ctypes.byref(h)) == 1      # head_dim must be 64
+    assert b"head_dim" in L.pkv_last_error(None)
+    assert L.pkv_create(16, 24, 16, 64, ctypes.byref(h)) == 1        # page_size
+    assert L.pkv_create(0, 256, 16, 64, ctypes.byref(h)) == 1        # empty pool
+    assert L.pkv_destroy(None) == 0
+    assert L.pkv_synth_fill(None, 1, 1, 1, 64, 0, 0, 0, 0, 0, 0, 0, 1.0, None) == 1
