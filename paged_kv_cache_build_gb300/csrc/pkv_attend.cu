@@ -77,6 +77,7 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int r, int c) {
   return base + r * 128 + (swizzle_chunk(r, c) << 4);
 }
 
+#ifdef PKV_ATTEND_MMA_SYNC
 __global__ void __launch_bounds__(kThreads) attend_mma_kernel(const AttendArgs a) {
   __shared__ __align__(1024) uint16_t sQ[kBM * kHeadDim];
   __shared__ __align__(1024) uint16_t sK[2][kBN * kHeadDim];
@@ -265,6 +266,8 @@ __global__ void __launch_bounds__(kThreads) attend_mma_kernel(const AttendArgs a
   }
 }
 
+#endif  // PKV_ATTEND_MMA_SYNC
+
 // Merge the splits' partial (o, m, l) of each (row, head): one warp per pair,
 // two head_dim elements per lane.
 __global__ void __launch_bounds__(256) combine_kernel(const AttendArgs a) {
@@ -295,19 +298,27 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttendArgs a) {
 }  // namespace
 
 int attend_num_splits(int n_q, int heads, int n_tiles, int num_sms) {
+#ifdef PKV_ATTEND_MMA_SYNC
   const int base = ((n_q + kBM - 1) / kBM) * heads;
   int s = (2 * num_sms + base - 1) / base;
   if (s > 16) s = 16;
   if (s > n_tiles) s = n_tiles;
   return s < 1 ? 1 : s;
+#else
+  return attend_tc_splits(n_q, heads, n_tiles, num_sms);
+#endif
 }
 
 cudaError_t launch_attend(const AttendArgs& a, int num_sms, cudaStream_t s) {
   (void)num_sms;
+#ifdef PKV_ATTEND_MMA_SYNC
   dim3 grid((a.n_q + kBM - 1) / kBM, a.heads, a.num_splits);
   attend_mma_kernel<<<grid, kThreads, 0, s>>>(a);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
+#else
+  cudaError_t e = launch_attend_tc(a, s);
+#endif
   if (e != cudaSuccess || a.num_splits == 1) return e;
   const long long pairs = (long long)a.n_q * a.heads;
   combine_kernel<<<(unsigned)((pairs + 7) / 8), 256, 0, s>>>(a);

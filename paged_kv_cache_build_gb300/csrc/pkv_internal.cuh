@@ -184,6 +184,9 @@ cudaError_t launch_reset_meta(const ResetMetaArgs& a, cudaStream_t s);
 cudaError_t launch_table(const TableArgs& a, cudaStream_t s);
 cudaError_t launch_attend(const AttendArgs& a, int num_sms, cudaStream_t s);
 int attend_num_splits(int n_q, int heads, int n_tiles, int num_sms);
+cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t s);
+int attend_tc_splits(int n_q, int heads, int n_tiles, int num_sms);
+int attend_tc_mt(int n_q);
 cudaError_t launch_synth(uint16_t* dst, int n_frames, int n_tokens, int heads, int head_dim,
                          unsigned long long key_base, int frame0, int token0, float scale,
                          cudaStream_t s);
