@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--mode", choices=["graph", "eager"], default="graph")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--profile-frames", type=int, default=0,
+                   help="run N frames of the stream once, eagerly, and exit (a small case for ncu)")
     return p.parse_args()
 
 
@@ -495,9 +497,38 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """N frames of the stream, eagerly, inputs for those frames only: one attend
+    launch per frame, frames >= 71 in steady state (no timing, nothing printed
+    but a line of counts)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_cache_build_gb300 import PagedKVCache, frame_stream_cfg, synth_fill
+    from synth import TENSOR_K, TENSOR_Q, TENSOR_V
+    w = workload()
+    n = args.profile_frames
+    q = torch.empty((n, w.frame_tokens, w.heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    k, v, out = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    synth_fill(q, 0, w.index, 0, 0, 0, TENSOR_Q, 0, w.q_scale)
+    synth_fill(k, 0, w.index, 0, 0, 0, TENSOR_K)
+    synth_fill(v, 0, w.index, 0, 0, 0, TENSOR_V)
+    cache = PagedKVCache(w.pool_pages, w.page_size, w.heads, w.head_dim)
+    sid = cache.open_stream(frame_stream_cfg(w.num_scale, w.window, w.n_patch, w.n_special))
+    for t in range(n):
+        cache.append_frame(sid, k[t], v[t])
+        cache.attend(q[t], sid, out=out[t], sm_scale=w.sm_scale)
+        cache.evict_window(sid)
+    torch.cuda.synchronize()
+    cache.sync()
+    print(json.dumps({"profile_frames": n, "visible": cache.visible_count(sid)}))
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.profile_frames:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

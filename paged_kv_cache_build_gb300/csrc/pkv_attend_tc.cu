@@ -9,14 +9,15 @@
 // One CTA computes, for one head, MT M-tiles of 128 query rows against a range of
 // 64-slot KV tiles of the visible table (split-KV partials are merged by the
 // combine kernel). Roles:
-//   warp 0       producer: one 1-D bulk copy (cp.async.bulk) per page block of a
+//   warp 2       producer: one 1-D bulk copy (cp.async.bulk) per page block of a
 //                tile into a 4-stage shared-memory ring. Pages are stored in the
 //                pool already 128-byte swizzled, so a block lands in shared memory
 //                as a ready tensor-core operand; no tensor map is needed.
-//   warp 1       MMA issuer (one thread): S_m = Q_m K^T into TMEM, then
+//   warp 3       MMA issuer (one thread): S_m = Q_m K^T into TMEM, then
 //                O_m += P_m V into TMEM, software-pipelined so that QK of tile j
 //                overlaps the softmax of tile j-1.
-//   warps 4..    one warpgroup per M-tile (a thread per query row): reads its S
+//   warps 4..    one warpgroup per M-tile (a thread per query row; warp 0 alone
+//                for a last M-tile of at most 32 valid rows): reads its S
 //                row from TMEM, masks invalid slots, keeps a running max (only
 //                raised when it grows by more than 2^8, so O rarely needs
 //                rescaling), writes P = 2^(S - m) as bf16 into shared memory and
@@ -51,6 +52,7 @@ struct __align__(1024) TcSmem {
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[MT];
+  uint64_t s_free[MT];
   uint64_t p_full[MT];
   uint64_t o_done[MT];
   uint64_t mma_done;
@@ -73,6 +75,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Non-blocking probe of a phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -217,8 +230,19 @@ __device__ __forceinline__ uint64_t tile_mask(const AttendArgs& a, int tile) {
   return mask;
 }
 
-template <int MT>
-__global__ void __launch_bounds__((4 + 4 * MT) * 32, 1)
+// Warp roles: warp 2 produces, warp 3 issues MMAs, warps 4.. are the softmax
+// warpgroups of M-tiles 0, 1, ... (warp w reads TMEM lane quarter w % 4). When
+// the last M-tile's valid rows fit in one 32-row lane quarter (LAST == 1, a
+// frame's 262 rows), that tile gets a single softmax warp: warp 0. This keeps
+// the block at 12 warps or fewer, i.e. at most 3 warps per SM sub-partition,
+// so each thread may use up to 168 registers.
+template <int MT, int LAST>
+constexpr int tc_threads() { return (LAST == 1 ? 4 * MT : 4 + 4 * MT) * 32; }
+constexpr int kProducerWarp = 2;
+constexpr int kMmaWarp = 3;
+
+template <int MT, int LAST>
+__global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
     attend_tc_kernel(const AttendArgs a, int n_mgroups) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem<MT>& sm = *reinterpret_cast<TcSmem<MT>*>(
@@ -244,7 +268,9 @@ __global__ void __launch_bounds__((4 + 4 * MT) * 32, 1)
     }
     for (int m = 0; m < MT; ++m) {
       mbar_init(&sm.s_full[m], 1);
-      mbar_init(&sm.p_full[m], 128);
+      const int arrivals = m == MT - 1 ? 32 * LAST : 128;
+      mbar_init(&sm.s_free[m], arrivals);
+      mbar_init(&sm.p_full[m], arrivals);
       mbar_init(&sm.o_done[m], 1);
     }
     mbar_init(&sm.mma_done, 1);
@@ -255,6 +281,12 @@ __global__ void __launch_bounds__((4 + 4 * MT) * 32, 1)
     uint4* kv = reinterpret_cast<uint4*>(&sm.k[0][0]);
     const int n16 = 2 * kStages * kBN * 128 / 16;     // k and v rings are contiguous
     for (int i = threadIdx.x; i < n16; i += blockDim.x) kv[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (LAST < 4) {
+      // rows of the last P tile that no softmax warp writes stay zero
+      uint4* pl = reinterpret_cast<uint4*>(&sm.p[MT - 1][32 * LAST * 128]);
+      for (int i = threadIdx.x; i < (128 - 32 * LAST) * 8; i += blockDim.x)
+        pl[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
     for (int i = threadIdx.x; i < MT * 128 * 8; i += blockDim.x) {
       const int m = i / (128 * 8), r = (i >> 3) & 127, c = i & 7;
       const int row = row0 + m * 128 + r;
@@ -265,7 +297,7 @@ __global__ void __launch_bounds__((4 + 4 * MT) * 32, 1)
     }
     fence_proxy_async();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
                      smem_u32(&sm.tmem_base)),
                  "r"(TmemCols<MT>::kAlloc));
@@ -277,7 +309,15 @@ __global__ void __launch_bounds__((4 + 4 * MT) * 32, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
 
-  if (warp == 0) {
+  int m = -1, wq = 0;                              // softmax role: M-tile and lane quarter
+  if (warp >= 4) {
+    m = (warp - 4) >> 2;
+    wq = warp & 3;
+  } else if (LAST == 1 && warp == 0) {
+    m = MT - 1;
+  }
+
+  if (warp == kProducerWarp) {
     // ================================================================ producer
     if (lane == 0) {
       int issued_tiles = 0;
@@ -323,66 +363,90 @@ __global__ void __launch_bounds__((4 + 4 * MT) * 32, 1)
       for (int j = issued_tiles - 1; j >= 0 && j >= issued_tiles - kStages; --j)
         mbar_wait(&sm.kv_full[j % kStages], (j / kStages) & 1, abort, a.err, false);
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ============================================================= MMA issuer
+    // Event-driven: each sweep issues every QK and PV whose inputs are ready,
+    // so a slow M-tile never holds back the others.
+    //   QK(m, j) needs tile j in shared memory and S_m released by the softmax
+    //            (it copies S_m to registers before doing any arithmetic);
+    //   PV(m, j) needs P_m of tile j written;
+    //   stage of tile j is released once PV(m, j) is issued for every m.
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16(128, kBN, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, kHeadDim, true);
-      bool ok = true;
-      for (int j = 0; j < nT && ok; ++j) {
-        const int s = j % kStages;
-        if (!mbar_wait(&sm.kv_full[s], (j / kStages) & 1, abort, a.err)) break;
-        tc_fence_after();
-        const int sp = (j + kStages - 1) % kStages;   // stage of tile j - 1
-        // S_m = Q_m K_j^T once the softmax has consumed S_m of tile j - 1
-        for (int m = 0; m < MT; ++m) {
-          if (j > 0) {
-            if (!mbar_wait(&sm.p_full[m], (j - 1) & 1, abort, a.err)) {
-              ok = false;
-              break;
-            }
+      int qk_next[MT], pv_next[MT];
+#pragma unroll
+      for (int m = 0; m < MT; ++m) qk_next[m] = pv_next[m] = 0;
+      int loaded = 0, released = 0, done = 0;
+      uint32_t idle = 0;
+      while (done < MT && !*abort) {
+        bool progress = false;
+        if (loaded < nT) {
+          int lo = nT;
+#pragma unroll
+          for (int m = 0; m < MT; ++m) lo = min(lo, qk_next[m]);
+          if (loaded <= lo + 1 &&
+              mbar_test_wait(&sm.kv_full[loaded % kStages], (loaded / kStages) & 1)) {
+            ++loaded;
+            progress = true;
             tc_fence_after();
           }
-          const uint32_t qa = smem_u32(&sm.q[m][0]), kb = smem_u32(&sm.k[s][0]);
-#pragma unroll
-          for (int kk = 0; kk < kHeadDim / 16; ++kk)
-            tc_mma(tmem + m * kBN, sdesc(qa + kk * 32), sdesc(kb + kk * 32), kIdQK, kk > 0);
-          tc_commit(&sm.s_full[m]);
         }
-        // O_m += P_m V_{j-1}
-        if (ok && j > 0) {
-          for (int m = 0; m < MT; ++m) {
-            const uint32_t pa = smem_u32(&sm.p[m][0]), vb = smem_u32(&sm.v[sp][0]);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const int j = qk_next[m];
+          if (j < loaded && (j == 0 || mbar_test_wait(&sm.s_free[m], (j - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t qa = smem_u32(&sm.q[m][0]);
+            const uint32_t kb = smem_u32(&sm.k[j % kStages][0]);
+#pragma unroll
+            for (int kk = 0; kk < kHeadDim / 16; ++kk)
+              tc_mma(tmem + m * kBN, sdesc(qa + kk * 32), sdesc(kb + kk * 32), kIdQK, kk > 0);
+            tc_commit(&sm.s_full[m]);
+            qk_next[m] = j + 1;
+            progress = true;
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const int j = pv_next[m];
+          if (j < qk_next[m] && mbar_test_wait(&sm.p_full[m], j & 1)) {
+            tc_fence_after();
+            const uint32_t pa = smem_u32(&sm.p[m][0]);
+            const uint32_t vb = smem_u32(&sm.v[j % kStages][0]);
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-              tc_mma(tmem + TmemCols<MT>::kO + m * kHeadDim, sdesc(pa + kk * 32), sdesc(vb + kk * 2048), kIdPV,
-                     (j > 1 || kk > 0) ? 1u : 0u);
+              tc_mma(tmem + TmemCols<MT>::kO + m * kHeadDim, sdesc(pa + kk * 32),
+                     sdesc(vb + kk * 2048), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
             tc_commit(&sm.o_done[m]);
+            pv_next[m] = j + 1;
+            if (j + 1 == nT) ++done;
+            progress = true;
           }
-          tc_commit(&sm.kv_empty[sp]);
         }
-      }
-      if (ok && nT > 0 && !*abort) {
-        const int jl = nT - 1, sl = jl % kStages;
-        for (int m = 0; m < MT; ++m) {
-          if (!mbar_wait(&sm.p_full[m], jl & 1, abort, a.err)) break;
-          tc_fence_after();
-          const uint32_t pa = smem_u32(&sm.p[m][0]), vb = smem_u32(&sm.v[sl][0]);
+        int lo = nT;
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            tc_mma(tmem + TmemCols<MT>::kO + m * kHeadDim, sdesc(pa + kk * 32), sdesc(vb + kk * 2048), kIdPV,
-                   (jl > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&sm.o_done[m]);
+        for (int m = 0; m < MT; ++m) lo = min(lo, pv_next[m]);
+        while (released < lo) {
+          tc_commit(&sm.kv_empty[released % kStages]);
+          ++released;
+        }
+        if (nT == 0) break;
+        if (progress) {
+          idle = 0;
+        } else if (++idle > kSpinLimit) {
+          atomicOr(a.err, kErrTimeout);
+          *abort = 1;
+        } else if ((idle & 255u) == 255u) {
+          __nanosleep(64);
         }
       }
       // every MMA issued by this thread has completed once mma_done flips
       tc_commit(&sm.mma_done);
       mbar_wait(&sm.mma_done, 0, abort, a.err, false);
     }
-  } else if (warp >= 4) {
+  } else if (m >= 0) {
     // ================================================================ softmax
-    const int m = (warp - 4) >> 2;
-    const int wq = warp & 3;                       // TMEM lane quarter of this warp
     const int r = wq * 32 + lane;                  // row inside the M-tile
     const int row = row0 + m * 128 + r;
     const bool warp_active = row0 + m * 128 + wq * 32 < a.n_q;
@@ -390,7 +454,8 @@ __global__ void __launch_bounds__((4 + 4 * MT) * 32, 1)
     const uint32_t t_s = tmem + t_lane + m * kBN;
     const uint32_t t_o = tmem + t_lane + TmemCols<MT>::kO + m * kHeadDim;
     uint8_t* p_row = &sm.p[m][r * 128];
-    float m_run = -INFINITY, l_run = 0.f;
+    const float sl2 = a.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;          // running max (log2 units) and sum
     bool alive = true;
     for (int j = 0; j < nT; ++j) {
       if (!mbar_wait(&sm.s_full[m], j & 1, abort, a.err)) {
@@ -398,24 +463,34 @@ __global__ void __launch_bounds__((4 + 4 * MT) * 32, 1)
         break;
       }
       tc_fence_after();
-      uint32_t packed[32];
       bool rescale = false;
       float alpha = 1.f;
+      float s[kBN];
       if (warp_active) {
-        const uint64_t mask = tile_mask(a, t0 + j);
-        float s[kBN];
 #pragma unroll
         for (int c = 0; c < kBN; c += 16) {
           uint32_t* rr = reinterpret_cast<uint32_t*>(&s[c]);
           PKV_TMEM_LD16(t_s + c, rr);
         }
         tmem_wait_ld();
-        float mx = -INFINITY;
+      }
+      // S_m is in registers: the next QK may overwrite it
+      tc_fence_before();
+      mbar_arrive(&sm.s_free[m]);
+      if (warp_active) {
+        const uint64_t mask = tile_mask(a, t0 + j);
+        if (mask != ~0ull) {
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          s[c] = ((mask >> c) & 1ull) ? s[c] * a.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, s[c]);
+          for (int c = 0; c < kBN; ++c)
+            if (!((mask >> c) & 1ull)) s[c] = -INFINITY;
         }
+        float mx0 = s[0], mx1 = s[1];
+#pragma unroll
+        for (int c = 2; c < kBN; c += 2) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+        }
+        const float mx = fmaxf(mx0, mx1) * sl2;      // sl2 > 0: max commutes with scaling
         const float m_new = fmaxf(m_run, mx);
         if (m_run == -INFINITY) {
           m_run = m_new;
@@ -426,20 +501,23 @@ __global__ void __launch_bounds__((4 + 4 * MT) * 32, 1)
           rescale = true;
         }
         const float m_ref = m_run == -INFINITY ? 0.f : m_run;
-        float sum = 0.f;
+        float sum0 = 0.f, sum1 = 0.f;
+        // P packed as bf16 pairs, compacted in place into s[0 .. kBN/2)
 #pragma unroll
         for (int c = 0; c < kBN; c += 2) {
-          const uint32_t pk = pack_bf16(fast_exp2(s[c] - m_ref), fast_exp2(s[c + 1] - m_ref));
-          packed[c >> 1] = pk;
-          __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&pk);
-          const float2 f = __bfloat1622float2(b);
-          sum += f.x + f.y;
+          const float p0 = fast_exp2(fmaf(s[c], sl2, -m_ref));
+          const float p1 = fast_exp2(fmaf(s[c + 1], sl2, -m_ref));
+          s[c >> 1] = __uint_as_float(pack_bf16(p0, p1));
+          sum0 += p0;
+          sum1 += p1;
         }
-        l_run += sum;
+        l_run += sum0 + sum1;
       } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) packed[c] = 0u;
+        for (int c = 0; c < kBN / 2; ++c) s[c] = 0.f;
       }
+      // PV of the previous tile must be done before P_m is overwritten and
+      // before O_m is rescaled
       if (j > 0) {
         if (!mbar_wait(&sm.o_done[m], (j - 1) & 1, abort, a.err)) {
           alive = false;
@@ -463,81 +541,81 @@ __global__ void __launch_bounds__((4 + 4 * MT) * 32, 1)
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         *reinterpret_cast<uint4*>(p_row + (swizzle_chunk(r, c) << 4)) =
-            make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+            make_uint4(__float_as_uint(s[4 * c]), __float_as_uint(s[4 * c + 1]),
+                       __float_as_uint(s[4 * c + 2]), __float_as_uint(s[4 * c + 3]));
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&sm.p_full[m]);
     }
-    // ---- epilogue
-    float o[kHeadDim];
-#pragma unroll
-    for (int c = 0; c < kHeadDim; ++c) o[c] = 0.f;
+    // ---- epilogue: O_m row to the output (or the split's partial), 16 columns at a time
+    bool have_o = false;
     if (alive && nT > 0) {
-      if (mbar_wait(&sm.o_done[m], (nT - 1) & 1, abort, a.err)) {
-        tc_fence_after();
-        if (warp_active) {
+      have_o = mbar_wait(&sm.o_done[m], (nT - 1) & 1, abort, a.err);
+      if (have_o) tc_fence_after();
+    }
+    const bool write = alive && row < a.n_q && (have_o || nT == 0);
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    const long long ro = ((long long)split * a.n_q + row) * H + h;
 #pragma unroll
-          for (int c = 0; c < kHeadDim; c += 16) {
-            uint32_t* rr = reinterpret_cast<uint32_t*>(&o[c]);
-            PKV_TMEM_LD16(t_o + c, rr);
-          }
-          tmem_wait_ld();
+    for (int c = 0; c < kHeadDim; c += 16) {
+      uint32_t o[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i] = 0u;
+      if (have_o && warp_active) {
+        PKV_TMEM_LD16(t_o + c, o);
+        tmem_wait_ld();
+      }
+      if (!write) continue;
+      if (a.num_splits == 1) {
+        uint4* dst = reinterpret_cast<uint4*>(a.out + ((long long)row * H + h) * kHeadDim + c);
+#pragma unroll
+        for (int q4 = 0; q4 < 2; ++q4) {
+          const float* f = reinterpret_cast<const float*>(&o[8 * q4]);
+          dst[q4] = make_uint4(pack_bf16(f[0] * inv, f[1] * inv), pack_bf16(f[2] * inv, f[3] * inv),
+                               pack_bf16(f[4] * inv, f[5] * inv), pack_bf16(f[6] * inv, f[7] * inv));
         }
       } else {
-        alive = false;
+        uint4* dst = reinterpret_cast<uint4*>(a.part_o + ro * kHeadDim + c);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          dst[q4] = make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
       }
     }
-    if (row < a.n_q && alive) {
-      if (a.num_splits == 1) {
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(a.out + ((long long)row * H + h) * kHeadDim);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          dst[c] = make_uint4(pack_bf16(o[8 * c] * inv, o[8 * c + 1] * inv),
-                              pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                              pack_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
-                              pack_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
-      } else {
-        const long long ro = ((long long)split * a.n_q + row) * H + h;
-        float4* dst = reinterpret_cast<float4*>(a.part_o + ro * kHeadDim);
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          dst[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-        *reinterpret_cast<float2*>(a.part_ml + ro * 2) = make_float2(m_run, l_run);
-      }
-    }
+    if (write && a.num_splits > 1)
+      *reinterpret_cast<float2*>(a.part_ml + ro * 2) = make_float2(m_run, l_run);
   }
 
   // ---- teardown: every role has finished its waits; free TMEM
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem),
                  "r"(TmemCols<MT>::kAlloc));
   }
 }
 
-template <int MT>
+template <int MT, int LAST>
 cudaError_t launch_mt(const AttendArgs& a, int n_mgroups, cudaStream_t s) {
   const size_t smem = sizeof(TcSmem<MT>) + 1024;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<MT>,
+    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<MT, LAST>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int grid = n_mgroups * a.heads * a.num_splits;
-  attend_tc_kernel<MT><<<grid, (4 + 4 * MT) * 32, smem, s>>>(a, n_mgroups);
+  attend_tc_kernel<MT, LAST><<<grid, tc_threads<MT, LAST>(), smem, s>>>(a, n_mgroups);
   count_launches(1);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-// M-tiles per CTA for n_q query rows.
-int attend_tc_mt(int n_q) { return n_q <= 128 ? 1 : (n_q <= 256 ? 2 : 3); }
+// M-tiles per CTA for n_q query rows: one M-group of up to three tiles when the
+// rows fit (a frame's tokens), else groups of two tiles (a chunk's tokens).
+int attend_tc_mt(int n_q) { return n_q <= 128 ? 1 : (n_q <= 256 ? 2 : (n_q <= 384 ? 3 : 2)); }
 
 // Split-KV factor: fill the SMs in as few, as even waves as possible.
 int attend_tc_splits(int n_q, int heads, int n_tiles, int num_sms) {
@@ -564,10 +642,15 @@ int attend_tc_splits(int n_q, int heads, int n_tiles, int num_sms) {
 cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t s) {
   const int mt = attend_tc_mt(a.n_q);
   const int n_mgroups = (a.n_q + mt * 128 - 1) / (mt * 128);
-  switch (mt) {
-    case 1: return launch_mt<1>(a, n_mgroups, s);
-    case 2: return launch_mt<2>(a, n_mgroups, s);
-    default: return launch_mt<3>(a, n_mgroups, s);
+  // one softmax warp for the last M-tile when a single M-group's last tile has <= 32 rows
+  const bool thin = n_mgroups == 1 && a.n_q - (mt - 1) * 128 <= 32;
+  switch (mt * 2 + (thin ? 1 : 0)) {
+    case 3: return launch_mt<1, 1>(a, n_mgroups, s);
+    case 2: return launch_mt<1, 4>(a, n_mgroups, s);
+    case 5: return launch_mt<2, 1>(a, n_mgroups, s);
+    case 4: return launch_mt<2, 4>(a, n_mgroups, s);
+    case 7: return launch_mt<3, 1>(a, n_mgroups, s);
+    default: return launch_mt<3, 4>(a, n_mgroups, s);
   }
 }
 
