@@ -297,15 +297,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttendArgs a) {
 
 }  // namespace
 
-int attend_num_splits(int n_q, int heads, int n_tiles, int num_sms) {
+int attend_num_splits(int n_q, int heads, long long n_slots, int num_sms) {
 #ifdef PKV_ATTEND_MMA_SYNC
+  const int n_tiles = (int)((n_slots + kBN - 1) / kBN);
   const int base = ((n_q + kBM - 1) / kBM) * heads;
   int s = (2 * num_sms + base - 1) / base;
   if (s > 16) s = 16;
   if (s > n_tiles) s = n_tiles;
   return s < 1 ? 1 : s;
 #else
-  return attend_tc_splits(n_q, heads, n_tiles, num_sms);
+  return attend_tc_splits(n_q, heads, attend_tc_tiles(n_slots), num_sms);
 #endif
 }
 

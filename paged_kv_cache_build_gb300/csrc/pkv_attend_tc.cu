@@ -6,22 +6,27 @@
 // vLLM-Omni RFC "Reconstruction Engine", section 3.3: a chunk's tokens attend over
 // the in-window chunks the same way.
 //
-// One CTA computes, for one head, MT M-tiles of 128 query rows against a range of
-// 64-slot KV tiles of the visible table (split-KV partials are merged by the
-// combine kernel). Roles:
+// One CTA computes, for one head, MT (1 or 2) M-tiles of 128 query rows, plus
+// up to 16 extra rows, against a range of 128-slot KV tiles of the visible
+// table (split-KV partials are merged by the combine kernel). A frame's 262
+// tokens are two M-tiles plus 6 extra rows. Roles:
 //   warp 2       producer: one 1-D bulk copy (cp.async.bulk) per page block of a
-//                tile into a 4-stage shared-memory ring. Pages are stored in the
-//                pool already 128-byte swizzled, so a block lands in shared memory
-//                as a ready tensor-core operand; no tensor map is needed.
-//   warp 3       MMA issuer (one thread): S_m = Q_m K^T into TMEM, then
-//                O_m += P_m V into TMEM, software-pipelined so that QK of tile j
-//                overlaps the softmax of tile j-1.
-//   warps 4..    one warpgroup per M-tile (a thread per query row; warp 0 alone
-//                for a last M-tile of at most 32 valid rows): reads its S
-//                row from TMEM, masks invalid slots, keeps a running max (only
-//                raised when it grows by more than 2^8, so O rarely needs
-//                rescaling), writes P = 2^(S - m) as bf16 into shared memory and
-//                finally reads O from TMEM.
+//                tile into a 4-stage shared-memory ring, plus the tile's 128-bit
+//                slot-validity mask. Pages are stored in the pool already
+//                128-byte swizzled, so a block lands in shared memory as a ready
+//                tensor-core operand; no tensor map is needed.
+//   warp 3       MMA issuer (one thread): S_m = Q_m K^T (N = 128 slots) and
+//                O_m += P_m V into TMEM, issued as soon as their inputs are ready.
+//   warps 4..    one warpgroup per M-tile (a thread per query row): copies its S
+//                row from TMEM to registers (freeing S for the next QK), masks
+//                invalid slots, keeps a running max (only raised when it grows by
+//                more than 2^8, so O rarely needs rescaling), writes P = 2^(S - m)
+//                as bf16 into shared memory and finally reads O from TMEM.
+//   warp 0       the extra rows (if any): the same tiles through warp-level
+//                mma.sync tiles of 16 rows, entirely in registers; an M=128
+//                tensor-core tile for 6 rows would cost as much as a full one.
+// The tensor cores take about as long for a 128x64x16 MMA as for a 128x128x16
+// one, so QK runs on 128-slot tiles (N = 128) to halve its instruction count.
 // Every mbarrier wait is bounded; a wait that gives up sets the device error
 // word, and the CTA drains its copies and MMAs and frees TMEM before returning.
 #include <cuda_bf16.h>
@@ -32,13 +37,14 @@ namespace pkv {
 
 namespace {
 
-constexpr int kBN = 64;            // slots per KV tile
+constexpr int kBN = 128;           // slots per KV tile
 constexpr int kStages = 4;         // KV ring depth
-// TMEM columns: S_m at 64m, O_m at 64*MT + 64m; the allocation is a power of two.
+constexpr int kXRows = 16;         // extra query rows handled with mma.sync
+// TMEM columns: S_m at 128m, O_m at 128*MT + 64m; the allocation is a power of two.
 template <int MT>
 struct TmemCols {
-  static constexpr int kO = 64 * MT;
-  static constexpr int kAlloc = MT == 1 ? 128 : (MT == 2 ? 256 : 512);
+  static constexpr int kO = 128 * MT;
+  static constexpr int kAlloc = MT == 1 ? 256 : 512;
 };
 constexpr uint32_t kSpinLimit = 1u << 25;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -46,13 +52,13 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units
 template <int MT>
 struct __align__(1024) TcSmem {
   uint8_t q[MT][128 * 128];          // Q_m: 128 rows x 64 bf16, 128B-swizzled
-  uint8_t k[kStages][kBN * 128];     // K tile: 64 slots x 64 bf16
+  uint8_t k[kStages][kBN * 128];     // K tile: 128 slots x 64 bf16
   uint8_t v[kStages][kBN * 128];
-  uint8_t p[MT][128 * 128];          // P_m: 128 rows x 64 slots bf16
+  uint8_t p[MT][2][128 * 128];       // P_m: two 64-slot atoms of 128 rows x 128 B
+  uint64_t mask[kStages][2];         // slot validity of the stage's tile
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[MT];
-  uint64_t s_free[MT];
   uint64_t p_full[MT];
   uint64_t o_done[MT];
   uint64_t mma_done;
@@ -203,47 +209,68 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Validity bits of the 64 columns of tile `tile`: slot f = 64*tile + c is valid
-// when its table entry exists and the slot is below that page's length.
-__device__ __forceinline__ uint64_t tile_mask(const AttendArgs& a, int tile) {
-  const int Ps = a.page_size;
-  uint64_t mask = 0;
-  if (Ps >= kBN) {
-    const int f0 = tile * kBN;
-    const int e = f0 / Ps, so = f0 - e * Ps;
-    if (e < a.n_entries) {
-      int n = __ldg(&a.tbl_len[e]) - so;
-      n = n < 0 ? 0 : (n > kBN ? kBN : n);
-      mask = n == kBN ? ~0ull : ((1ull << n) - 1ull);
-    }
-  } else {
-    const int per = kBN / Ps;
-    for (int pp = 0; pp < per; ++pp) {
-      const int e = tile * per + pp;
-      if (e >= a.n_entries) break;
-      int n = __ldg(&a.tbl_len[e]);
-      n = n < 0 ? 0 : (n > Ps ? Ps : n);
-      const uint64_t bits = n >= 64 ? ~0ull : ((1ull << n) - 1ull);
-      mask |= bits << (pp * Ps);
-    }
-  }
-  return mask;
+// Legacy warp-level tensor-core helpers for the extra rows.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// shared address of logical 16-byte chunk c of row r of a [rows][64] swizzled tile
+__device__ __forceinline__ uint32_t sw_addr(uint32_t base, int r, int c) {
+  return base + r * 128 + (swizzle_chunk(r, c) << 4);
 }
 
-// Warp roles: warp 2 produces, warp 3 issues MMAs, warps 4.. are the softmax
-// warpgroups of M-tiles 0, 1, ... (warp w reads TMEM lane quarter w % 4). When
-// the last M-tile's valid rows fit in one 32-row lane quarter (LAST == 1, a
-// frame's 262 rows), that tile gets a single softmax warp: warp 0. This keeps
-// the block at 12 warps or fewer, i.e. at most 3 warps per SM sub-partition,
-// so each thread may use up to 168 registers.
-template <int MT, int LAST>
-constexpr int tc_threads() { return (LAST == 1 ? 4 * MT : 4 + 4 * MT) * 32; }
+// Slot-validity mask of a 128-slot tile: slot f = 128*tile + c is valid when its
+// table entry exists and the slot is below that page's length.
+__device__ __forceinline__ void tile_mask(const AttendArgs& a, int tile, uint64_t& lo,
+                                          uint64_t& hi) {
+  const int Ps = a.page_size;
+  lo = hi = 0;
+  const int per = Ps >= kBN ? 1 : kBN / Ps;
+  const int rows = Ps >= kBN ? kBN : Ps;
+  for (int pp = 0; pp < per; ++pp) {
+    const int f0 = tile * kBN + pp * rows;
+    const int e = f0 / Ps, so = f0 - e * Ps;
+    if (e >= a.n_entries) break;
+    int n = __ldg(&a.tbl_len[e]) - so;
+    n = n < 0 ? 0 : (n > rows ? rows : n);
+    const int b0 = pp * rows;                    // first bit of this block
+    // set bits [b0, b0 + n)
+    for (int half = 0; half < 2; ++half) {
+      const int lo_bit = max(b0, half * 64), hi_bit = min(b0 + n, half * 64 + 64);
+      if (hi_bit <= lo_bit) continue;
+      const int cnt = hi_bit - lo_bit;
+      const uint64_t bits = (cnt == 64 ? ~0ull : ((1ull << cnt) - 1ull)) << (lo_bit - half * 64);
+      if (half) hi |= bits;
+      else lo |= bits;
+    }
+  }
+}
+
+template <int MT, bool EXTRA>
+constexpr int tc_threads() { return (4 + 4 * MT) * 32; }
+constexpr int kXWarp = 0;
 constexpr int kProducerWarp = 2;
 constexpr int kMmaWarp = 3;
 
-template <int MT, int LAST>
-__global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
-    attend_tc_kernel(const AttendArgs a, int n_mgroups) {
+template <int MT, bool EXTRA>
+__global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
+    attend_tc_kernel(const AttendArgs a, int n_mgroups, int n_tiles) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem<MT>& sm = *reinterpret_cast<TcSmem<MT>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -255,8 +282,8 @@ __global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
   bid /= n_mgroups;
   const int h = bid % H;
   const int split = bid / H;
-  const int t0 = (int)((long long)a.n_tiles * split / a.num_splits);
-  const int t1 = (int)((long long)a.n_tiles * (split + 1) / a.num_splits);
+  const int t0 = (int)((long long)n_tiles * split / a.num_splits);
+  const int t1 = (int)((long long)n_tiles * (split + 1) / a.num_splits);
   const int nT = t1 - t0;
   const int row0 = mg * MT * 128;
 
@@ -264,13 +291,11 @@ __global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
+      mbar_init(&sm.kv_empty[s], EXTRA ? 2 : 1);
     }
     for (int m = 0; m < MT; ++m) {
       mbar_init(&sm.s_full[m], 1);
-      const int arrivals = m == MT - 1 ? 32 * LAST : 128;
-      mbar_init(&sm.s_free[m], arrivals);
-      mbar_init(&sm.p_full[m], arrivals);
+      mbar_init(&sm.p_full[m], 128);
       mbar_init(&sm.o_done[m], 1);
     }
     mbar_init(&sm.mma_done, 1);
@@ -281,12 +306,6 @@ __global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
     uint4* kv = reinterpret_cast<uint4*>(&sm.k[0][0]);
     const int n16 = 2 * kStages * kBN * 128 / 16;     // k and v rings are contiguous
     for (int i = threadIdx.x; i < n16; i += blockDim.x) kv[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (LAST < 4) {
-      // rows of the last P tile that no softmax warp writes stay zero
-      uint4* pl = reinterpret_cast<uint4*>(&sm.p[MT - 1][32 * LAST * 128]);
-      for (int i = threadIdx.x; i < (128 - 32 * LAST) * 8; i += blockDim.x)
-        pl[i] = make_uint4(0u, 0u, 0u, 0u);
-    }
     for (int i = threadIdx.x; i < MT * 128 * 8; i += blockDim.x) {
       const int m = i / (128 * 8), r = (i >> 3) & 127, c = i & 7;
       const int row = row0 + m * 128 + r;
@@ -309,27 +328,23 @@ __global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
 
-  int m = -1, wq = 0;                              // softmax role: M-tile and lane quarter
-  if (warp >= 4) {
-    m = (warp - 4) >> 2;
-    wq = warp & 3;
-  } else if (LAST == 1 && warp == 0) {
-    m = MT - 1;
-  }
-
   if (warp == kProducerWarp) {
     // ================================================================ producer
     if (lane == 0) {
       int issued_tiles = 0;
+      const int per = Ps >= kBN ? 1 : kBN / Ps;
+      const int rows = Ps >= kBN ? kBN : Ps;
       for (int j = 0; j < nT; ++j) {
         const int s = j % kStages;
         if (!mbar_wait(&sm.kv_empty[s], ((j / kStages) & 1) ^ 1, abort, a.err)) break;
         const int tile = t0 + j;
-        const int per = Ps >= kBN ? 1 : kBN / Ps;
-        const int rows = Ps >= kBN ? kBN : Ps;
+        uint64_t mlo, mhi;
+        tile_mask(a, tile, mlo, mhi);
+        sm.mask[s][0] = mlo;
+        sm.mask[s][1] = mhi;
         uint32_t bytes = 0;
         for (int pp = 0; pp < per; ++pp)
-          if (tile * kBN / Ps + pp < a.n_entries) bytes += 2u * rows * 128u;
+          if ((tile * kBN + pp * rows) / Ps < a.n_entries) bytes += 2u * rows * 128u;
         mbar_arrive_expect_tx(&sm.kv_full[s], bytes);
         for (int pp = 0; pp < per; ++pp) {
           const int f0 = tile * kBN + pp * rows;
@@ -365,12 +380,11 @@ __global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
     }
   } else if (warp == kMmaWarp) {
     // ============================================================= MMA issuer
-    // Event-driven: each sweep issues every QK and PV whose inputs are ready,
-    // so a slow M-tile never holds back the others.
-    //   QK(m, j) needs tile j in shared memory and S_m released by the softmax
-    //            (it copies S_m to registers before doing any arithmetic);
-    //   PV(m, j) needs P_m of tile j written;
-    //   stage of tile j is released once PV(m, j) is issued for every m.
+    // Event-driven: each sweep issues every QK and PV whose inputs are ready.
+    //   PV(m, j) needs P_m of tile j written (which also means S_m was read);
+    //   QK(m, j+1) needs tile j+1 in shared memory and PV(m, j) issued (S_m free);
+    //   the stage of tile j is released (one of its arrivals) once PV(m, j) has
+    //   been issued for every m and those MMAs complete.
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16(128, kBN, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, kHeadDim, true);
@@ -379,7 +393,7 @@ __global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
       for (int m = 0; m < MT; ++m) qk_next[m] = pv_next[m] = 0;
       int loaded = 0, released = 0, done = 0;
       uint32_t idle = 0;
-      while (done < MT && !*abort) {
+      while (done < MT && !*abort && nT > 0) {
         bool progress = false;
         if (loaded < nT) {
           int lo = nT;
@@ -395,13 +409,13 @@ __global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           const int j = qk_next[m];
-          if (j < loaded && (j == 0 || mbar_test_wait(&sm.s_free[m], (j - 1) & 1))) {
+          if (j < loaded && (j == 0 || pv_next[m] >= j)) {
             tc_fence_after();
-            const uint32_t qa = smem_u32(&sm.q[m][0]);
-            const uint32_t kb = smem_u32(&sm.k[j % kStages][0]);
+            const uint64_t qa = sdesc(smem_u32(&sm.q[m][0]));
+            const uint64_t kb = sdesc(smem_u32(&sm.k[j % kStages][0]));
 #pragma unroll
             for (int kk = 0; kk < kHeadDim / 16; ++kk)
-              tc_mma(tmem + m * kBN, sdesc(qa + kk * 32), sdesc(kb + kk * 32), kIdQK, kk > 0);
+              tc_mma(tmem + m * kBN, qa + 2 * kk, kb + 2 * kk, kIdQK, kk > 0);
             tc_commit(&sm.s_full[m]);
             qk_next[m] = j + 1;
             progress = true;
@@ -412,12 +426,14 @@ __global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
           const int j = pv_next[m];
           if (j < qk_next[m] && mbar_test_wait(&sm.p_full[m], j & 1)) {
             tc_fence_after();
-            const uint32_t pa = smem_u32(&sm.p[m][0]);
-            const uint32_t vb = smem_u32(&sm.v[j % kStages][0]);
+            const uint64_t pa0 = sdesc(smem_u32(&sm.p[m][0][0]));
+            const uint64_t pa1 = sdesc(smem_u32(&sm.p[m][1][0]));
+            const uint64_t vb = sdesc(smem_u32(&sm.v[j % kStages][0]));
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-              tc_mma(tmem + TmemCols<MT>::kO + m * kHeadDim, sdesc(pa + kk * 32),
-                     sdesc(vb + kk * 2048), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+              tc_mma(tmem + TmemCols<MT>::kO + m * kHeadDim,
+                     (kk < 4 ? pa0 : pa1) + 2 * (kk & 3), vb + 128 * kk, kIdPV,
+                     (j > 0 || kk > 0) ? 1u : 0u);
             tc_commit(&sm.o_done[m]);
             pv_next[m] = j + 1;
             if (j + 1 == nT) ++done;
@@ -431,7 +447,6 @@ __global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
           tc_commit(&sm.kv_empty[released % kStages]);
           ++released;
         }
-        if (nT == 0) break;
         if (progress) {
           idle = 0;
         } else if (++idle > kSpinLimit) {
@@ -445,52 +460,61 @@ __global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
       tc_commit(&sm.mma_done);
       mbar_wait(&sm.mma_done, 0, abort, a.err, false);
     }
-  } else if (m >= 0) {
+  } else if (warp >= 4) {
     // ================================================================ softmax
+    const int m = (warp - 4) >> 2;
+    const int wq = warp & 3;                       // TMEM lane quarter of this warp
     const int r = wq * 32 + lane;                  // row inside the M-tile
     const int row = row0 + m * 128 + r;
     const bool warp_active = row0 + m * 128 + wq * 32 < a.n_q;
     const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
     const uint32_t t_s = tmem + t_lane + m * kBN;
     const uint32_t t_o = tmem + t_lane + TmemCols<MT>::kO + m * kHeadDim;
-    uint8_t* p_row = &sm.p[m][r * 128];
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;          // running max (log2 units) and sum
     bool alive = true;
     for (int j = 0; j < nT; ++j) {
+      const int st = j % kStages;
       if (!mbar_wait(&sm.s_full[m], j & 1, abort, a.err)) {
         alive = false;
         break;
       }
       tc_fence_after();
+      // the stage's slot mask (its tile cannot be replaced before this P is used)
+      if (!mbar_wait(&sm.kv_full[st], (j / kStages) & 1, abort, a.err)) {
+        alive = false;
+        break;
+      }
+      const uint64_t mlo = sm.mask[st][0], mhi = sm.mask[st][1];
+      const bool full = (mlo & mhi) == ~0ull;
       bool rescale = false;
       float alpha = 1.f;
-      float s[kBN];
+      // pass 1: row max over the tile, 32 columns at a time
       if (warp_active) {
+        float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kBN; c += 16) {
-          uint32_t* rr = reinterpret_cast<uint32_t*>(&s[c]);
-          PKV_TMEM_LD16(t_s + c, rr);
-        }
-        tmem_wait_ld();
-      }
-      // S_m is in registers: the next QK may overwrite it
-      tc_fence_before();
-      mbar_arrive(&sm.s_free[m]);
-      if (warp_active) {
-        const uint64_t mask = tile_mask(a, t0 + j);
-        if (mask != ~0ull) {
+        for (int c0 = 0; c0 < kBN; c0 += 32) {
+          float v[32];
+          PKV_TMEM_LD16(t_s + c0, reinterpret_cast<uint32_t*>(&v[0]));
+          PKV_TMEM_LD16(t_s + c0 + 16, reinterpret_cast<uint32_t*>(&v[16]));
+          tmem_wait_ld();
+          if (!full) {
+            const uint32_t bits = (uint32_t)(((c0 < 64 ? mlo : mhi) >> (c0 & 63)) & 0xFFFFFFFFull);
 #pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (!((mask >> c) & 1ull)) s[c] = -INFINITY;
-        }
-        float mx0 = s[0], mx1 = s[1];
+            for (int c = 0; c < 32; ++c)
+              if (!((bits >> c) & 1u)) v[c] = -INFINITY;
+          }
+          float a0 = v[0], a1 = v[1], a2 = v[2], a3 = v[3];
 #pragma unroll
-        for (int c = 2; c < kBN; c += 2) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
+          for (int c = 4; c < 32; c += 4) {
+            a0 = fmaxf(a0, v[c]);
+            a1 = fmaxf(a1, v[c + 1]);
+            a2 = fmaxf(a2, v[c + 2]);
+            a3 = fmaxf(a3, v[c + 3]);
+          }
+          mx = fmaxf(mx, fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)));
         }
-        const float mx = fmaxf(mx0, mx1) * sl2;      // sl2 > 0: max commutes with scaling
+        mx *= sl2;                                 // sl2 > 0: max commutes with the scale
         const float m_new = fmaxf(m_run, mx);
         if (m_run == -INFINITY) {
           m_run = m_new;
@@ -500,21 +524,6 @@ __global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
           m_run = m_new;
           rescale = true;
         }
-        const float m_ref = m_run == -INFINITY ? 0.f : m_run;
-        float sum0 = 0.f, sum1 = 0.f;
-        // P packed as bf16 pairs, compacted in place into s[0 .. kBN/2)
-#pragma unroll
-        for (int c = 0; c < kBN; c += 2) {
-          const float p0 = fast_exp2(fmaf(s[c], sl2, -m_ref));
-          const float p1 = fast_exp2(fmaf(s[c + 1], sl2, -m_ref));
-          s[c >> 1] = __uint_as_float(pack_bf16(p0, p1));
-          sum0 += p0;
-          sum1 += p1;
-        }
-        l_run += sum0 + sum1;
-      } else {
-#pragma unroll
-        for (int c = 0; c < kBN / 2; ++c) s[c] = 0.f;
       }
       // PV of the previous tile must be done before P_m is overwritten and
       // before O_m is rescaled
@@ -538,11 +547,44 @@ __global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
         }
         tmem_wait_st();
       }
+      // pass 2: P = 2^(S*scale - m) as bf16 into the swizzled P tile, 32 columns at a time
+      const float m_ref = m_run == -INFINITY ? 0.f : m_run;
+      float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(p_row + (swizzle_chunk(r, c) << 4)) =
-            make_uint4(__float_as_uint(s[4 * c]), __float_as_uint(s[4 * c + 1]),
-                       __float_as_uint(s[4 * c + 2]), __float_as_uint(s[4 * c + 3]));
+      for (int c0 = 0; c0 < kBN; c0 += 32) {
+        uint32_t pk[16];
+        if (warp_active) {
+          float v[32];
+          PKV_TMEM_LD16(t_s + c0, reinterpret_cast<uint32_t*>(&v[0]));
+          PKV_TMEM_LD16(t_s + c0 + 16, reinterpret_cast<uint32_t*>(&v[16]));
+          tmem_wait_ld();
+          if (!full) {
+            const uint32_t bits = (uint32_t)(((c0 < 64 ? mlo : mhi) >> (c0 & 63)) & 0xFFFFFFFFull);
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (!((bits >> c) & 1u)) v[c] = -INFINITY;
+          }
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float p0 = fast_exp2(fmaf(v[c], sl2, -m_ref));
+            const float p1 = fast_exp2(fmaf(v[c + 1], sl2, -m_ref));
+            pk[c >> 1] = pack_bf16(p0, p1);
+            sum0 += p0;
+            sum1 += p1;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) pk[c] = 0u;
+        }
+        uint8_t* p_row = &sm.p[m][c0 >> 6][r * 128];
+        const int cb = (c0 & 63) >> 3;             // first 16-byte chunk of this block
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(p_row + (swizzle_chunk(r, cb + c) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
+      l_run += sum0 + sum1;
+      // S_m has been read and P_m written: QK(m, j+1) and PV(m, j) may go
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&sm.p_full[m]);
@@ -583,6 +625,137 @@ __global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
     }
     if (write && a.num_splits > 1)
       *reinterpret_cast<float2*>(a.part_ml + ro * 2) = make_float2(m_run, l_run);
+  } else if (EXTRA && warp == kXWarp) {
+    // ============================================== extra rows (mma.sync, regs)
+    const int xr0 = row0 + MT * 128;               // first extra row
+    const int g = lane >> 2, tq = lane & 3;
+    // Q fragments (rows xr0 + g and xr0 + g + 8), zero beyond n_q
+    uint32_t qa[4][4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rr = xr0 + g + (i & 1) * 8;
+        const int d = kk * 16 + (i >> 1) * 8 + 2 * tq;
+        qa[kk][i] = rr < a.n_q
+                        ? __ldg(reinterpret_cast<const uint32_t*>(a.q + ((long long)rr * H + h) * kHeadDim + d))
+                        : 0u;
+      }
+    float m_x[2] = {-INFINITY, -INFINITY}, l_x[2] = {0.f, 0.f};
+    float ox[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ox[i][0] = ox[i][1] = ox[i][2] = ox[i][3] = 0.f;
+    const float sl2 = a.scale_log2;
+    bool alive = true;
+    for (int j = 0; j < nT; ++j) {
+      const int st = j % kStages;
+      if (!mbar_wait(&sm.kv_full[st], (j / kStages) & 1, abort, a.err)) {
+        alive = false;
+        break;
+      }
+      const uint32_t kbase = smem_u32(&sm.k[st][0]), vbase = smem_u32(&sm.v[st][0]);
+      // the tile in two 64-slot halves, each one online-softmax step
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const uint64_t mbits = sm.mask[st][half];
+        float sx[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sx[i][0] = sx[i][1] = sx[i][2] = sx[i][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+          for (int np = 0; np < 4; ++np) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(sw_addr(kbase, half * 64 + np * 16 + (lane & 7) + (lane >> 4) * 8,
+                            2 * kk + ((lane >> 3) & 1)),
+                    b0, b1, b2, b3);
+            mma_16816(sx[2 * np], qa[kk], b0, b1);
+            mma_16816(sx[2 * np + 1], qa[kk], b2, b3);
+          }
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int col = nt * 8 + 2 * tq + (e & 1);
+            sx[nt][e] = ((mbits >> col) & 1ull) ? sx[nt][e] * sl2 : -INFINITY;
+            mx[e >> 1] = fmaxf(mx[e >> 1], sx[nt][e]);
+          }
+        float alpha[2], m_use[2];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+          mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+          const float m_new = fmaxf(m_x[rr], mx[rr]);
+          m_use[rr] = m_new == -INFINITY ? 0.f : m_new;
+          alpha[rr] = fast_exp2(m_x[rr] - m_use[rr]);
+          m_x[rr] = m_new;
+        }
+        float rs[2] = {0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float pv = fast_exp2(sx[nt][e] - m_use[e >> 1]);
+            sx[nt][e] = pv;
+            rs[e >> 1] += pv;
+          }
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) l_x[rr] = l_x[rr] * alpha[rr] + rs[rr];
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt) {
+          ox[dt][0] *= alpha[0];
+          ox[dt][1] *= alpha[0];
+          ox[dt][2] *= alpha[1];
+          ox[dt][3] *= alpha[1];
+        }
+        // O += P V (k = slots of this half), V through transposed ldmatrix
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t pa[4];
+          pa[0] = pack_bf16(sx[2 * kk][0], sx[2 * kk][1]);
+          pa[1] = pack_bf16(sx[2 * kk][2], sx[2 * kk][3]);
+          pa[2] = pack_bf16(sx[2 * kk + 1][0], sx[2 * kk + 1][1]);
+          pa[3] = pack_bf16(sx[2 * kk + 1][2], sx[2 * kk + 1][3]);
+#pragma unroll
+          for (int dp = 0; dp < 4; ++dp) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(sw_addr(vbase, half * 64 + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8,
+                              2 * dp + (lane >> 4)),
+                      b0, b1, b2, b3);
+            mma_16816(ox[2 * dp], pa, b0, b1);
+            mma_16816(ox[2 * dp + 1], pa, b2, b3);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.kv_empty[st]);
+    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      l_x[rr] += __shfl_xor_sync(0xffffffffu, l_x[rr], 1);
+      l_x[rr] += __shfl_xor_sync(0xffffffffu, l_x[rr], 2);
+    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int xrow = xr0 + g + rr * 8;
+      if (!alive || xrow >= a.n_q) continue;
+      if (a.num_splits == 1) {
+        const float inv = l_x[rr] > 0.f ? 1.f / l_x[rr] : 0.f;
+        uint16_t* dst = a.out + ((long long)xrow * H + h) * kHeadDim;
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt)
+          *reinterpret_cast<uint32_t*>(dst + dt * 8 + 2 * tq) =
+              pack_bf16(ox[dt][2 * rr] * inv, ox[dt][2 * rr + 1] * inv);
+      } else {
+        const long long ro = ((long long)split * a.n_q + xrow) * H + h;
+        float* dst = a.part_o + ro * kHeadDim;
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt)
+          *reinterpret_cast<float2*>(dst + dt * 8 + 2 * tq) = make_float2(ox[dt][2 * rr], ox[dt][2 * rr + 1]);
+        if (tq == 0) *reinterpret_cast<float2*>(a.part_ml + ro * 2) = make_float2(m_x[rr], l_x[rr]);
+      }
+    }
   }
 
   // ---- teardown: every role has finished its waits; free TMEM
@@ -595,37 +768,50 @@ __global__ void __launch_bounds__(tc_threads<MT, LAST>(), 1)
   }
 }
 
-template <int MT, int LAST>
-cudaError_t launch_mt(const AttendArgs& a, int n_mgroups, cudaStream_t s) {
+template <int MT, bool EXTRA>
+cudaError_t launch_mt(const AttendArgs& a, int n_mgroups, int n_tiles, cudaStream_t s) {
   const size_t smem = sizeof(TcSmem<MT>) + 1024;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<MT, LAST>,
+    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<MT, EXTRA>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int grid = n_mgroups * a.heads * a.num_splits;
-  attend_tc_kernel<MT, LAST><<<grid, tc_threads<MT, LAST>(), smem, s>>>(a, n_mgroups);
+  attend_tc_kernel<MT, EXTRA><<<grid, tc_threads<MT, EXTRA>(), smem, s>>>(a, n_mgroups, n_tiles);
   count_launches(1);
   return cudaGetLastError();
 }
 
+struct TcShape {
+  int mt, n_mgroups;
+  bool extra;
+};
+
+// Query rows per CTA: up to two 128-row M-tiles, plus up to 16 extra rows when
+// the whole query fits one group that way (a frame's 256 + 6 tokens); longer
+// queries (a chunk's tokens) are cut into groups of 256 rows.
+TcShape tc_shape(int n_q) {
+  if (n_q <= 128) return {1, 1, false};
+  if (n_q <= 128 + kXRows) return {1, 1, true};
+  if (n_q <= 256) return {2, 1, false};
+  if (n_q <= 256 + kXRows) return {2, 1, true};
+  return {2, (n_q + 255) / 256, false};
+}
+
 }  // namespace
 
-// M-tiles per CTA for n_q query rows: one M-group of up to three tiles when the
-// rows fit (a frame's tokens), else groups of two tiles (a chunk's tokens).
-int attend_tc_mt(int n_q) { return n_q <= 128 ? 1 : (n_q <= 256 ? 2 : (n_q <= 384 ? 3 : 2)); }
+int attend_tc_tiles(long long n_slots) { return (int)((n_slots + kBN - 1) / kBN); }
 
 // Split-KV factor: fill the SMs in as few, as even waves as possible.
 int attend_tc_splits(int n_q, int heads, int n_tiles, int num_sms) {
-  const int mt = attend_tc_mt(n_q);
-  const int groups = (n_q + mt * 128 - 1) / (mt * 128);
-  const int base = groups * heads;
+  const TcShape sh = tc_shape(n_q);
+  const int base = sh.n_mgroups * heads;
   int best = 1;
   double best_eff = 0.0;
   for (int s = 1; s <= 16; ++s) {
-    if (s > 1 && n_tiles / s < 4) break;
+    if (s > 1 && n_tiles / s < 3) break;
     const int ctas = base * s;
     const int waves = (ctas + num_sms - 1) / num_sms;
     // a wave's time is proportional to the tiles each CTA handles
@@ -640,18 +826,14 @@ int attend_tc_splits(int n_q, int heads, int n_tiles, int num_sms) {
 }
 
 cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t s) {
-  const int mt = attend_tc_mt(a.n_q);
-  const int n_mgroups = (a.n_q + mt * 128 - 1) / (mt * 128);
-  // one softmax warp for the last M-tile when a single M-group's last tile has <= 32 rows
-  const bool thin = n_mgroups == 1 && a.n_q - (mt - 1) * 128 <= 32;
-  switch (mt * 2 + (thin ? 1 : 0)) {
-    case 3: return launch_mt<1, 1>(a, n_mgroups, s);
-    case 2: return launch_mt<1, 4>(a, n_mgroups, s);
-    case 5: return launch_mt<2, 1>(a, n_mgroups, s);
-    case 4: return launch_mt<2, 4>(a, n_mgroups, s);
-    case 7: return launch_mt<3, 1>(a, n_mgroups, s);
-    default: return launch_mt<3, 4>(a, n_mgroups, s);
+  const TcShape sh = tc_shape(a.n_q);
+  const int n_tiles = attend_tc_tiles(a.n_slots);
+  if (sh.mt == 1) {
+    return sh.extra ? launch_mt<1, true>(a, sh.n_mgroups, n_tiles, s)
+                    : launch_mt<1, false>(a, sh.n_mgroups, n_tiles, s);
   }
+  return sh.extra ? launch_mt<2, true>(a, sh.n_mgroups, n_tiles, s)
+                  : launch_mt<2, false>(a, sh.n_mgroups, n_tiles, s);
 }
 
 }  // namespace pkv

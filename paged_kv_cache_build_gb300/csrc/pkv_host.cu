@@ -762,10 +762,11 @@ static pkv_status attend_common(pkv_t h, Stream* st, const void* q, int n_q, int
   a.tbl_idx = st->d_tbl_idx;
   a.tbl_len = st->d_tbl_len;
   a.n_entries = np;
-  a.n_tiles = ceil_div((long long)(np - 1) * h->Ps + last, 64);
+  a.n_slots = (long long)(np - 1) * h->Ps + last;
+  a.n_tiles = ceil_div(a.n_slots, 64);
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)h->D);
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.num_splits = attend_num_splits(n_q, h->H, a.n_tiles, h->num_sms);
+  a.num_splits = attend_num_splits(n_q, h->H, a.n_slots, h->num_sms);
   a.err = h->d_err;
   if (a.num_splits > 1) {
     const size_t o_bytes = (size_t)a.num_splits * n_q * h->H * kHeadDim * sizeof(float);

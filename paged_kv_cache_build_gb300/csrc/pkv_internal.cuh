@@ -164,6 +164,7 @@ struct AttendArgs {
   const int32_t* tbl_len;
   int n_entries;
   int n_tiles;                      // 64-slot tiles covering the table's slots
+  long long n_slots;                // flat slots up to the last valid one
   float scale_log2;                 // sm_scale * log2(e)
   int num_splits;
   float* part_o;                    // [split][n_q][heads][64]
@@ -183,10 +184,10 @@ cudaError_t launch_reset_copy(const ResetCopyArgs& a, cudaStream_t s);
 cudaError_t launch_reset_meta(const ResetMetaArgs& a, cudaStream_t s);
 cudaError_t launch_table(const TableArgs& a, cudaStream_t s);
 cudaError_t launch_attend(const AttendArgs& a, int num_sms, cudaStream_t s);
-int attend_num_splits(int n_q, int heads, int n_tiles, int num_sms);
+int attend_num_splits(int n_q, int heads, long long n_slots, int num_sms);
 cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t s);
 int attend_tc_splits(int n_q, int heads, int n_tiles, int num_sms);
-int attend_tc_mt(int n_q);
+int attend_tc_tiles(long long n_slots);
 cudaError_t launch_synth(uint16_t* dst, int n_frames, int n_tokens, int heads, int head_dim,
                          unsigned long long key_base, int frame0, int token0, float scale,
                          cudaStream_t s);
