@@ -47,7 +47,7 @@ struct TmemCols {
   static constexpr int kAlloc = MT == 1 ? 256 : 512;
 };
 constexpr uint32_t kSpinLimit = 1u << 25;
-constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr float kOverflowGuard = 64.0f;     // log2 units: p stays below 2^64
 
 template <int MT>
 struct __align__(1024) TcSmem {
@@ -181,6 +181,17 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),     \
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
         "=r"(r[14]), "=r"(r[15])                                                                 \
+      : "r"(taddr))
+
+#define PKV_TMEM_LD32(taddr, r)                                                                  \
+  asm volatile(                                                                                  \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"   \
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"      \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),     \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),           \
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),           \
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])            \
       : "r"(taddr))
 
 #define PKV_TMEM_ST16(taddr, r)                                                                  \
@@ -381,16 +392,17 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   } else if (warp == kMmaWarp) {
     // ============================================================= MMA issuer
     // Event-driven: each sweep issues every QK and PV whose inputs are ready.
-    //   PV(m, j) needs P_m of tile j written (which also means S_m was read);
-    //   QK(m, j+1) needs tile j+1 in shared memory and PV(m, j) issued (S_m free);
+    //   QK(m, j+1) needs tile j+1 in shared memory and P_m of tile j written
+    //   (which means S_m was read); it goes out before PV(m, j), which needs the
+    //   same P_m, so that the softmax can start on tile j+1 sooner;
     //   the stage of tile j is released (one of its arrivals) once PV(m, j) has
     //   been issued for every m and those MMAs complete.
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16(128, kBN, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, kHeadDim, true);
-      int qk_next[MT], pv_next[MT];
+      int qk_next[MT], pv_next[MT], p_seen[MT];
 #pragma unroll
-      for (int m = 0; m < MT; ++m) qk_next[m] = pv_next[m] = 0;
+      for (int m = 0; m < MT; ++m) qk_next[m] = pv_next[m] = p_seen[m] = 0;
       int loaded = 0, released = 0, done = 0;
       uint32_t idle = 0;
       while (done < MT && !*abort && nT > 0) {
@@ -408,35 +420,37 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
         }
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-          const int j = qk_next[m];
-          if (j < loaded && (j == 0 || pv_next[m] >= j)) {
+          // P_m of tile p_seen[m] written (and S_m read) by the softmax
+          if (p_seen[m] < qk_next[m] && mbar_test_wait(&sm.p_full[m], p_seen[m] & 1)) {
+            ++p_seen[m];
+            progress = true;
             tc_fence_after();
+          }
+          // QK(m, j) first: it restarts the softmax; PV(m, j - 1) follows
+          const int jq = qk_next[m];
+          if (jq < loaded && p_seen[m] >= jq) {
             const uint64_t qa = sdesc(smem_u32(&sm.q[m][0]));
-            const uint64_t kb = sdesc(smem_u32(&sm.k[j % kStages][0]));
+            const uint64_t kb = sdesc(smem_u32(&sm.k[jq % kStages][0]));
 #pragma unroll
             for (int kk = 0; kk < kHeadDim / 16; ++kk)
               tc_mma(tmem + m * kBN, qa + 2 * kk, kb + 2 * kk, kIdQK, kk > 0);
             tc_commit(&sm.s_full[m]);
-            qk_next[m] = j + 1;
+            qk_next[m] = jq + 1;
             progress = true;
           }
-        }
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          const int j = pv_next[m];
-          if (j < qk_next[m] && mbar_test_wait(&sm.p_full[m], j & 1)) {
-            tc_fence_after();
+          const int jp = pv_next[m];
+          if (jp < p_seen[m]) {
             const uint64_t pa0 = sdesc(smem_u32(&sm.p[m][0][0]));
             const uint64_t pa1 = sdesc(smem_u32(&sm.p[m][1][0]));
-            const uint64_t vb = sdesc(smem_u32(&sm.v[j % kStages][0]));
+            const uint64_t vb = sdesc(smem_u32(&sm.v[jp % kStages][0]));
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
               tc_mma(tmem + TmemCols<MT>::kO + m * kHeadDim,
                      (kk < 4 ? pa0 : pa1) + 2 * (kk & 3), vb + 128 * kk, kIdPV,
-                     (j > 0 || kk > 0) ? 1u : 0u);
+                     (jp > 0 || kk > 0) ? 1u : 0u);
             tc_commit(&sm.o_done[m]);
-            pv_next[m] = j + 1;
-            if (j + 1 == nT) ++done;
+            pv_next[m] = jp + 1;
+            if (jp + 1 == nT) ++done;
             progress = true;
           }
         }
@@ -487,44 +501,95 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
       }
       const uint64_t mlo = sm.mask[st][0], mhi = sm.mask[st][1];
       const bool full = (mlo & mhi) == ~0ull;
+      // Fast path: exponentiate against the running max of the earlier tiles and
+      // track this tile's max on the way, 64 columns at a time. Any reference
+      // keeps the result exact (it cancels in O / l); it only has to keep
+      // 2^(s - m) finite, so the exact path (tile max first, O rescaled) runs on
+      // the first tile and when the max has grown by more than 2^64.
+      uint32_t pk[kBN / 2];                        // P row as bf16 pairs
       bool rescale = false;
       float alpha = 1.f;
-      // pass 1: row max over the tile, 32 columns at a time
-      if (warp_active) {
-        float mx = -INFINITY;
+      float sum0 = 0.f, sum1 = 0.f;
+      bool redo = m_run == -INFINITY;
+      if (warp_active && !redo) {
+        const float m_ref = m_run;
+        float t0m = -INFINITY, t1m = -INFINITY;
 #pragma unroll
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
-          float v[32];
-          PKV_TMEM_LD16(t_s + c0, reinterpret_cast<uint32_t*>(&v[0]));
-          PKV_TMEM_LD16(t_s + c0 + 16, reinterpret_cast<uint32_t*>(&v[16]));
+        for (int hf = 0; hf < 2; ++hf) {
+          float v[64];
+          PKV_TMEM_LD32(t_s + 64 * hf, reinterpret_cast<uint32_t*>(&v[0]));
+          PKV_TMEM_LD32(t_s + 64 * hf + 32, reinterpret_cast<uint32_t*>(&v[32]));
           tmem_wait_ld();
+          const uint64_t bits = hf ? mhi : mlo;
           if (!full) {
-            const uint32_t bits = (uint32_t)(((c0 < 64 ? mlo : mhi) >> (c0 & 63)) & 0xFFFFFFFFull);
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (!((bits >> c) & 1u)) v[c] = -INFINITY;
+            for (int c = 0; c < 64; ++c)
+              if (!((bits >> c) & 1ull)) v[c] = -INFINITY;
           }
-          float a0 = v[0], a1 = v[1], a2 = v[2], a3 = v[3];
 #pragma unroll
-          for (int c = 4; c < 32; c += 4) {
-            a0 = fmaxf(a0, v[c]);
-            a1 = fmaxf(a1, v[c + 1]);
-            a2 = fmaxf(a2, v[c + 2]);
-            a3 = fmaxf(a3, v[c + 3]);
+          for (int c = 0; c < 64; c += 2) {
+            t0m = fmaxf(t0m, v[c]);
+            t1m = fmaxf(t1m, v[c + 1]);
+            const float p0 = fast_exp2(fmaf(v[c], sl2, -m_ref));
+            const float p1 = fast_exp2(fmaf(v[c + 1], sl2, -m_ref));
+            pk[32 * hf + (c >> 1)] = pack_bf16(p0, p1);
+            sum0 += p0;
+            sum1 += p1;
           }
-          mx = fmaxf(mx, fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)));
         }
-        mx *= sl2;                                 // sl2 > 0: max commutes with the scale
-        const float m_new = fmaxf(m_run, mx);
-        if (m_run == -INFINITY) {
+        redo = fmaxf(t0m, t1m) * sl2 > m_ref + kOverflowGuard;
+      }
+      if (__any_sync(0xffffffffu, warp_active && redo)) {
+        // exact path for the whole warp: S again from TMEM (QK(m, j+1) waits for P)
+        if (warp_active) {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            float v[64];
+            PKV_TMEM_LD32(t_s + 64 * hf, reinterpret_cast<uint32_t*>(&v[0]));
+            PKV_TMEM_LD32(t_s + 64 * hf + 32, reinterpret_cast<uint32_t*>(&v[32]));
+            tmem_wait_ld();
+            const uint64_t bits = hf ? mhi : mlo;
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if ((bits >> c) & 1ull) mx = fmaxf(mx, v[c]);
+          }
+          mx *= sl2;                               // sl2 > 0: max commutes with the scale
+          const float m_new = fmaxf(m_run, mx);
+          if (m_run != -INFINITY && m_new > m_run) {
+            alpha = fast_exp2(m_run - m_new);
+            l_run *= alpha;
+            rescale = true;
+          }
           m_run = m_new;
-        } else if (m_new > m_run + kRescaleThreshold) {
-          alpha = fast_exp2(m_run - m_new);
-          l_run *= alpha;
-          m_run = m_new;
-          rescale = true;
+          const float m_ref = m_run == -INFINITY ? 0.f : m_run;
+          sum0 = sum1 = 0.f;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            float v[64];
+            PKV_TMEM_LD32(t_s + 64 * hf, reinterpret_cast<uint32_t*>(&v[0]));
+            PKV_TMEM_LD32(t_s + 64 * hf + 32, reinterpret_cast<uint32_t*>(&v[32]));
+            tmem_wait_ld();
+            const uint64_t bits = hf ? mhi : mlo;
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (!((bits >> c) & 1ull)) v[c] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+              const float p0 = fast_exp2(fmaf(v[c], sl2, -m_ref));
+              const float p1 = fast_exp2(fmaf(v[c + 1], sl2, -m_ref));
+              pk[32 * hf + (c >> 1)] = pack_bf16(p0, p1);
+              sum0 += p0;
+              sum1 += p1;
+            }
+          }
         }
       }
+      if (!warp_active) {
+#pragma unroll
+        for (int c = 0; c < kBN / 2; ++c) pk[c] = 0u;
+      }
+      l_run += sum0 + sum1;
       // PV of the previous tile must be done before P_m is overwritten and
       // before O_m is rescaled
       if (j > 0) {
@@ -547,43 +612,17 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
         }
         tmem_wait_st();
       }
-      // pass 2: P = 2^(S*scale - m) as bf16 into the swizzled P tile, 32 columns at a time
-      const float m_ref = m_run == -INFINITY ? 0.f : m_run;
-      float sum0 = 0.f, sum1 = 0.f;
+      // P row (bf16, two 64-slot atoms) into the swizzled P tile
 #pragma unroll
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
-        uint32_t pk[16];
-        if (warp_active) {
-          float v[32];
-          PKV_TMEM_LD16(t_s + c0, reinterpret_cast<uint32_t*>(&v[0]));
-          PKV_TMEM_LD16(t_s + c0 + 16, reinterpret_cast<uint32_t*>(&v[16]));
-          tmem_wait_ld();
-          if (!full) {
-            const uint32_t bits = (uint32_t)(((c0 < 64 ? mlo : mhi) >> (c0 & 63)) & 0xFFFFFFFFull);
+      for (int at = 0; at < 2; ++at) {
+        uint8_t* p_row = &sm.p[m][at][r * 128];
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (!((bits >> c) & 1u)) v[c] = -INFINITY;
-          }
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float p0 = fast_exp2(fmaf(v[c], sl2, -m_ref));
-            const float p1 = fast_exp2(fmaf(v[c + 1], sl2, -m_ref));
-            pk[c >> 1] = pack_bf16(p0, p1);
-            sum0 += p0;
-            sum1 += p1;
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) pk[c] = 0u;
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t* q4 = &pk[at * 32 + 4 * c];
+          *reinterpret_cast<uint4*>(p_row + (swizzle_chunk(r, c) << 4)) =
+              make_uint4(q4[0], q4[1], q4[2], q4[3]);
         }
-        uint8_t* p_row = &sm.p[m][c0 >> 6][r * 128];
-        const int cb = (c0 & 63) >> 3;             // first 16-byte chunk of this block
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(p_row + (swizzle_chunk(r, cb + c) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       }
-      l_run += sum0 + sum1;
       // S_m has been read and P_m written: QK(m, j+1) and PV(m, j) may go
       fence_proxy_async();
       tc_fence_before();
