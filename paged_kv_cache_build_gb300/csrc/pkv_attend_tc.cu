@@ -400,9 +400,9 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16(128, kBN, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, kHeadDim, true);
-      int qk_next[MT], pv_next[MT], p_seen[MT], pv_kk[MT];
+      int qk_next[MT], pv_next[MT], p_seen[MT];
 #pragma unroll
-      for (int m = 0; m < MT; ++m) qk_next[m] = pv_next[m] = p_seen[m] = pv_kk[m] = 0;
+      for (int m = 0; m < MT; ++m) qk_next[m] = pv_next[m] = p_seen[m] = 0;
       int loaded = 0, released = 0, done = 0;
       uint32_t idle = 0;
       while (done < MT && !*abort && nT > 0) {
@@ -439,27 +439,22 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
             progress = true;
           }
         }
-        // then PV, two k-steps at a time: the tensor core runs MMAs in issue
-        // order, so a QK that becomes ready waits behind at most two of them
+        // then PV(m, j) for every P_m that is ready
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           const int jp = pv_next[m];
           if (jp < p_seen[m]) {
-            const uint64_t pa = sdesc(smem_u32(&sm.p[m][pv_kk[m] >> 2][0]));
+            const uint64_t pa0 = sdesc(smem_u32(&sm.p[m][0][0]));
+            const uint64_t pa1 = sdesc(smem_u32(&sm.p[m][1][0]));
             const uint64_t vb = sdesc(smem_u32(&sm.v[jp % kStages][0]));
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int kk = pv_kk[m] + u;
-              tc_mma(tmem + TmemCols<MT>::kO + m * kHeadDim, pa + 2 * (kk & 3), vb + 128 * kk,
-                     kIdPV, (jp > 0 || kk > 0) ? 1u : 0u);
-            }
-            pv_kk[m] += 2;
-            if (pv_kk[m] == kBN / 16) {
-              tc_commit(&sm.o_done[m]);
-              pv_kk[m] = 0;
-              pv_next[m] = jp + 1;
-              if (jp + 1 == nT) ++done;
-            }
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              tc_mma(tmem + TmemCols<MT>::kO + m * kHeadDim,
+                     (kk < 4 ? pa0 : pa1) + 2 * (kk & 3), vb + 128 * kk, kIdPV,
+                     (jp > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(&sm.o_done[m]);
+            pv_next[m] = jp + 1;
+            if (jp + 1 == nT) ++done;
             progress = true;
           }
         }
