@@ -15,8 +15,8 @@
 //                slot-validity mask. Pages are stored in the pool already
 //                128-byte swizzled, so a block lands in shared memory as a ready
 //                tensor-core operand; no tensor map is needed.
-//   warp 3       MMA issuer (one thread): S_m = Q_m K^T (N = 128 slots) and
-//                O_m += P_m V into TMEM, issued as soon as their inputs are ready.
+//   warps 3, 1   MMA issuers (one thread each, one per M-tile): S_m = Q_m K^T
+//                (N = 128 slots) and O_m += P_m V into TMEM.
 //   warps 4..    one warpgroup per M-tile (a thread per query row): copies its S
 //                row from TMEM to registers (freeing S for the next QK), masks
 //                invalid slots, keeps a running max (only raised when it grows by
@@ -61,7 +61,7 @@ struct __align__(1024) TcSmem {
   uint64_t s_full[MT];
   uint64_t p_full[MT];
   uint64_t o_done[MT];
-  uint64_t mma_done;
+  uint64_t mma_done[MT];
   uint32_t tmem_base;
   int abort;
 };
@@ -277,7 +277,8 @@ template <int MT, bool EXTRA>
 constexpr int tc_threads() { return (4 + 4 * MT) * 32; }
 constexpr int kXWarp = 0;
 constexpr int kProducerWarp = 2;
-constexpr int kMmaWarp = 3;
+constexpr int kMmaWarp = 3;          // MMA issuer of M-tile 0 (and TMEM owner)
+constexpr int kMmaWarp2 = 1;         // MMA issuer of M-tile 1
 
 template <int MT, bool EXTRA>
 __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
@@ -302,14 +303,14 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.kv_empty[s], EXTRA ? 2 : 1);
+      mbar_init(&sm.kv_empty[s], MT + (EXTRA ? 1 : 0));   // one per MMA issuer (+ extra warp)
     }
     for (int m = 0; m < MT; ++m) {
       mbar_init(&sm.s_full[m], 1);
       mbar_init(&sm.p_full[m], 128);
       mbar_init(&sm.o_done[m], 1);
     }
-    mbar_init(&sm.mma_done, 1);
+    for (int m = 0; m < MT; ++m) mbar_init(&sm.mma_done[m], 1);
     sm.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -389,94 +390,53 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
       for (int j = issued_tiles - 1; j >= 0 && j >= issued_tiles - kStages; --j)
         mbar_wait(&sm.kv_full[j % kStages], (j / kStages) & 1, abort, a.err, false);
     }
-  } else if (warp == kMmaWarp) {
-    // ============================================================= MMA issuer
-    // Event-driven: each sweep issues every QK and PV whose inputs are ready.
-    //   QK(m, j+1) needs tile j+1 in shared memory and P_m of tile j written
-    //   (which means S_m was read); it goes out before PV(m, j), which needs the
-    //   same P_m, so that the softmax can start on tile j+1 sooner;
-    //   the stage of tile j is released (one of its arrivals) once PV(m, j) has
-    //   been issued for every m and those MMAs complete.
+  } else if (warp == kMmaWarp || (MT == 2 && warp == kMmaWarp2)) {
+    // ============================================================ MMA issuers
+    // One issuing thread per M-tile (warp 3: M-tile 0; warp 1: M-tile 1). An
+    // issuing thread stalls on each tcgen05.mma until the tensor core accepts
+    // it, so a single issuer for both M-tiles would make each M-tile's next QK
+    // wait behind the other's PV. Per M-tile, in order:
+    //   QK(m, j)    tile j in shared memory, and P_m of tile j-1 written (the
+    //               softmax has read S_m);
+    //   PV(m, j-1)  right after: it finishes while the softmax works on tile j,
+    //               which needs it done only before overwriting P_m;
+    //   then one arrival on the stage of tile j-1 when those MMAs complete.
     if (lane == 0) {
+      const int m = warp == kMmaWarp ? 0 : 1;
       constexpr uint32_t kIdQK = idesc_bf16(128, kBN, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, kHeadDim, true);
-      int qk_next[MT], pv_next[MT], p_seen[MT];
-#pragma unroll
-      for (int m = 0; m < MT; ++m) qk_next[m] = pv_next[m] = p_seen[m] = 0;
-      int loaded = 0, released = 0, done = 0;
-      uint32_t idle = 0;
-      while (done < MT && !*abort && nT > 0) {
-        bool progress = false;
-        if (loaded < nT) {
-          int lo = nT;
-#pragma unroll
-          for (int m = 0; m < MT; ++m) lo = min(lo, qk_next[m]);
-          if (loaded <= lo + 1 &&
-              mbar_test_wait(&sm.kv_full[loaded % kStages], (loaded / kStages) & 1)) {
-            ++loaded;
-            progress = true;
-            tc_fence_after();
-          }
+      const uint64_t qa = sdesc(smem_u32(&sm.q[m][0]));
+      const uint64_t pa0 = sdesc(smem_u32(&sm.p[m][0][0]));
+      const uint64_t pa1 = sdesc(smem_u32(&sm.p[m][1][0]));
+      for (int j = 0; j <= nT && nT > 0; ++j) {
+        if (j < nT) {
+          if (!mbar_wait(&sm.kv_full[j % kStages], (j / kStages) & 1, abort, a.err)) break;
         }
-        // QKs first: each one restarts a softmax warpgroup
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          // P_m of tile p_seen[m] written (and S_m read) by the softmax
-          if (p_seen[m] < qk_next[m] && mbar_test_wait(&sm.p_full[m], p_seen[m] & 1)) {
-            ++p_seen[m];
-            progress = true;
-            tc_fence_after();
-          }
-          const int jq = qk_next[m];
-          if (jq < loaded && p_seen[m] >= jq) {
-            const uint64_t qa = sdesc(smem_u32(&sm.q[m][0]));
-            const uint64_t kb = sdesc(smem_u32(&sm.k[jq % kStages][0]));
-#pragma unroll
-            for (int kk = 0; kk < kHeadDim / 16; ++kk)
-              tc_mma(tmem + m * kBN, qa + 2 * kk, kb + 2 * kk, kIdQK, kk > 0);
-            tc_commit(&sm.s_full[m]);
-            qk_next[m] = jq + 1;
-            progress = true;
-          }
+        if (j > 0) {
+          if (!mbar_wait(&sm.p_full[m], (j - 1) & 1, abort, a.err)) break;
         }
-        // then PV(m, j) for every P_m that is ready
+        tc_fence_after();
+        if (j < nT) {
+          const uint64_t kb = sdesc(smem_u32(&sm.k[j % kStages][0]));
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          const int jp = pv_next[m];
-          if (jp < p_seen[m]) {
-            const uint64_t pa0 = sdesc(smem_u32(&sm.p[m][0][0]));
-            const uint64_t pa1 = sdesc(smem_u32(&sm.p[m][1][0]));
-            const uint64_t vb = sdesc(smem_u32(&sm.v[jp % kStages][0]));
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              tc_mma(tmem + TmemCols<MT>::kO + m * kHeadDim,
-                     (kk < 4 ? pa0 : pa1) + 2 * (kk & 3), vb + 128 * kk, kIdPV,
-                     (jp > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(&sm.o_done[m]);
-            pv_next[m] = jp + 1;
-            if (jp + 1 == nT) ++done;
-            progress = true;
-          }
+          for (int kk = 0; kk < kHeadDim / 16; ++kk)
+            tc_mma(tmem + m * kBN, qa + 2 * kk, kb + 2 * kk, kIdQK, kk > 0);
+          tc_commit(&sm.s_full[m]);
         }
-        int lo = nT;
+        if (j > 0) {
+          const int jp = j - 1;
+          const uint64_t vb = sdesc(smem_u32(&sm.v[jp % kStages][0]));
 #pragma unroll
-        for (int m = 0; m < MT; ++m) lo = min(lo, pv_next[m]);
-        while (released < lo) {
-          tc_commit(&sm.kv_empty[released % kStages]);
-          ++released;
-        }
-        if (progress) {
-          idle = 0;
-        } else if (++idle > kSpinLimit) {
-          atomicOr(a.err, kErrTimeout);
-          *abort = 1;
-        } else if ((idle & 255u) == 255u) {
-          __nanosleep(64);
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            tc_mma(tmem + TmemCols<MT>::kO + m * kHeadDim, (kk < 4 ? pa0 : pa1) + 2 * (kk & 3),
+                   vb + 128 * kk, kIdPV, (jp > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&sm.o_done[m]);
+          tc_commit(&sm.kv_empty[jp % kStages]);
         }
       }
-      // every MMA issued by this thread has completed once mma_done flips
-      tc_commit(&sm.mma_done);
-      mbar_wait(&sm.mma_done, 0, abort, a.err, false);
+      // every MMA issued by this thread has completed once mma_done[m] flips
+      tc_commit(&sm.mma_done[m]);
+      mbar_wait(&sm.mma_done[m], 0, abort, a.err, false);
     }
   } else if (warp >= 4) {
     // ================================================================ softmax
