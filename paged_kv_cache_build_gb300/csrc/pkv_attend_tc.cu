@@ -22,8 +22,8 @@
 //                invalid slots, keeps a running max (only raised when it grows by
 //                more than 2^8, so O rarely needs rescaling), writes P = 2^(S - m)
 //                as bf16 into shared memory and finally reads O from TMEM.
-//   warp 0       the extra rows (if any): the same tiles through warp-level
-//                mma.sync tiles of 16 rows, entirely in registers; an M=128
+//   warp 0       the extra rows (at most 8, if any): the same tiles through
+//                warp-level mma.sync tiles, entirely in registers; an M=128
 //                tensor-core tile for 6 rows would cost as much as a full one.
 // The tensor cores take about as long for a 128x64x16 MMA as for a 128x128x16
 // one, so QK runs on 128-slot tiles (N = 128) to halve its instruction count.
@@ -39,7 +39,7 @@ namespace {
 
 constexpr int kBN = 128;           // slots per KV tile
 constexpr int kStages = 4;         // KV ring depth
-constexpr int kXRows = 16;         // extra query rows handled with mma.sync
+constexpr int kXRows = 8;          // extra query rows handled with mma.sync
 // TMEM columns: S_m at 128m, O_m at 128*MT + 64m; the allocation is a power of two.
 template <int MT>
 struct TmemCols {
@@ -630,24 +630,31 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
       *reinterpret_cast<float2*>(a.part_ml + ro * 2) = make_float2(m_run, l_run);
   } else if (EXTRA && warp == kXWarp) {
     // ============================================== extra rows (mma.sync, regs)
+    // Up to 8 query rows, transposed so that the 8 queries are the N = 8 side of
+    // m16n8k16 tiles and the slots the M = 16 side: S^T = K Q_x^T (8 tiles of
+    // 16 slots per 128-slot tile), then O^T += V^T P^T with P^T moved into B
+    // fragments by movmatrix. Softmax runs over slots, i.e. across the 8 lanes
+    // that share a query column.
     const int xr0 = row0 + MT * 128;               // first extra row
     const int g = lane >> 2, tq = lane & 3;
-    // Q fragments (rows xr0 + g and xr0 + g + 8), zero beyond n_q
-    uint32_t qa[4][4];
+    // B fragments of Q_x^T: (k = d 2tq.., n = query g)
+    uint32_t qb[4][2];
+    {
+      const int qrow = xr0 + g;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
+      for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int rr = xr0 + g + (i & 1) * 8;
-        const int d = kk * 16 + (i >> 1) * 8 + 2 * tq;
-        qa[kk][i] = rr < a.n_q
-                        ? __ldg(reinterpret_cast<const uint32_t*>(a.q + ((long long)rr * H + h) * kHeadDim + d))
-                        : 0u;
-      }
+        for (int i = 0; i < 2; ++i)
+          qb[kk][i] = qrow < a.n_q ? __ldg(reinterpret_cast<const uint32_t*>(
+                                         a.q + ((long long)qrow * H + h) * kHeadDim + kk * 16 +
+                                         i * 8 + 2 * tq))
+                                   : 0u;
+    }
+    // per thread: queries 2tq and 2tq+1
     float m_x[2] = {-INFINITY, -INFINITY}, l_x[2] = {0.f, 0.f};
-    float ox[8][4];
+    float ox[4][4];                                // O^T: d-tile x (d g|g+8, query 2tq|2tq+1)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) ox[i][0] = ox[i][1] = ox[i][2] = ox[i][3] = 0.f;
+    for (int i = 0; i < 4; ++i) ox[i][0] = ox[i][1] = ox[i][2] = ox[i][3] = 0.f;
     const float sl2 = a.scale_log2;
     bool alive = true;
     for (int j = 0; j < nT; ++j) {
@@ -656,108 +663,101 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
         alive = false;
         break;
       }
+      const uint64_t mlo = sm.mask[st][0], mhi = sm.mask[st][1];
       const uint32_t kbase = smem_u32(&sm.k[st][0]), vbase = smem_u32(&sm.v[st][0]);
-      // the tile in two 64-slot halves, each one online-softmax step
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        const uint64_t mbits = sm.mask[st][half];
-        float sx[8][4];
+      // S^T (128 slots x 8 queries) in 8 slot-tiles of 16
+      float sc[8][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sx[i][0] = sx[i][1] = sx[i][2] = sx[i][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-          for (int np = 0; np < 4; ++np) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(sw_addr(kbase, half * 64 + np * 16 + (lane & 7) + (lane >> 4) * 8,
-                            2 * kk + ((lane >> 3) & 1)),
-                    b0, b1, b2, b3);
-            mma_16816(sx[2 * np], qa[kk], b0, b1);
-            mma_16816(sx[2 * np + 1], qa[kk], b2, b3);
-          }
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int col = nt * 8 + 2 * tq + (e & 1);
-            sx[nt][e] = ((mbits >> col) & 1ull) ? sx[nt][e] * sl2 : -INFINITY;
-            mx[e >> 1] = fmaxf(mx[e >> 1], sx[nt][e]);
-          }
-        float alpha[2], m_use[2];
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
-          mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
-          const float m_new = fmaxf(m_x[rr], mx[rr]);
-          m_use[rr] = m_new == -INFINITY ? 0.f : m_new;
-          alpha[rr] = fast_exp2(m_x[rr] - m_use[rr]);
-          m_x[rr] = m_new;
-        }
-        float rs[2] = {0.f, 0.f};
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float pv = fast_exp2(sx[nt][e] - m_use[e >> 1]);
-            sx[nt][e] = pv;
-            rs[e >> 1] += pv;
-          }
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) l_x[rr] = l_x[rr] * alpha[rr] + rs[rr];
-#pragma unroll
-        for (int dt = 0; dt < 8; ++dt) {
-          ox[dt][0] *= alpha[0];
-          ox[dt][1] *= alpha[0];
-          ox[dt][2] *= alpha[1];
-          ox[dt][3] *= alpha[1];
-        }
-        // O += P V (k = slots of this half), V through transposed ldmatrix
+      for (int mt = 0; mt < 8; ++mt) {
+        sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          uint32_t pa[4];
-          pa[0] = pack_bf16(sx[2 * kk][0], sx[2 * kk][1]);
-          pa[1] = pack_bf16(sx[2 * kk][2], sx[2 * kk][3]);
-          pa[2] = pack_bf16(sx[2 * kk + 1][0], sx[2 * kk + 1][1]);
-          pa[3] = pack_bf16(sx[2 * kk + 1][2], sx[2 * kk + 1][3]);
+          uint32_t ka[4];
+          ldsm_x4(sw_addr(kbase, mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * kk + (lane >> 4)),
+                  ka[0], ka[1], ka[2], ka[3]);
+          mma_16816(sc[mt], ka, qb[kk][0], qb[kk][1]);
+        }
+      }
+      // mask, scale, per-query max over the tile's slots
+      float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-          for (int dp = 0; dp < 4; ++dp) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(sw_addr(vbase, half * 64 + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8,
-                              2 * dp + (lane >> 4)),
-                      b0, b1, b2, b3);
-            mma_16816(ox[2 * dp], pa, b0, b1);
-            mma_16816(ox[2 * dp + 1], pa, b2, b3);
-          }
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int slot = mt * 16 + g + (e >> 1) * 8;
+          const bool ok = ((slot < 64 ? mlo : mhi) >> (slot & 63)) & 1ull;
+          sc[mt][e] = ok ? sc[mt][e] * sl2 : -INFINITY;
+          mx[e & 1] = fmaxf(mx[e & 1], sc[mt][e]);
+        }
+      float alpha[2], m_use[2];
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        mx[qq] = fmaxf(mx[qq], __shfl_xor_sync(0xffffffffu, mx[qq], 4));
+        mx[qq] = fmaxf(mx[qq], __shfl_xor_sync(0xffffffffu, mx[qq], 8));
+        mx[qq] = fmaxf(mx[qq], __shfl_xor_sync(0xffffffffu, mx[qq], 16));
+        const float m_new = fmaxf(m_x[qq], mx[qq]);
+        m_use[qq] = m_new == -INFINITY ? 0.f : m_new;
+        alpha[qq] = fast_exp2(m_x[qq] - m_use[qq]);
+        m_x[qq] = m_new;
+        l_x[qq] *= alpha[qq];
+      }
+#pragma unroll
+      for (int dt = 0; dt < 4; ++dt) {
+        ox[dt][0] *= alpha[0];
+        ox[dt][1] *= alpha[1];
+        ox[dt][2] *= alpha[0];
+        ox[dt][3] *= alpha[1];
+      }
+      // P^T, then O^T += V^T P^T per 16-slot k-step
+#pragma unroll
+      for (int kp = 0; kp < 8; ++kp) {
+        const float p0 = fast_exp2(sc[kp][0] - m_use[0]);
+        const float p1 = fast_exp2(sc[kp][1] - m_use[1]);
+        const float p2 = fast_exp2(sc[kp][2] - m_use[0]);
+        const float p3 = fast_exp2(sc[kp][3] - m_use[1]);
+        l_x[0] += p0 + p2;
+        l_x[1] += p1 + p3;
+        // (slot g | g+8, query 2tq..) pairs -> transposed: (query g, slots 2tq..)
+        uint32_t pb0 = pack_bf16(p0, p1), pb1 = pack_bf16(p2, p3);
+        asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %0;\n" : "+r"(pb0));
+        asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %0;\n" : "+r"(pb1));
+#pragma unroll
+        for (int dt = 0; dt < 4; ++dt) {
+          uint32_t va[4];
+          ldsm_x4_t(sw_addr(vbase, kp * 16 + (lane & 7) + (lane >> 4) * 8, 2 * dt + ((lane >> 3) & 1)),
+                    va[0], va[1], va[2], va[3]);
+          mma_16816(ox[dt], va, pb0, pb1);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.kv_empty[st]);
     }
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      l_x[rr] += __shfl_xor_sync(0xffffffffu, l_x[rr], 1);
-      l_x[rr] += __shfl_xor_sync(0xffffffffu, l_x[rr], 2);
+    for (int qq = 0; qq < 2; ++qq) {
+      l_x[qq] += __shfl_xor_sync(0xffffffffu, l_x[qq], 4);
+      l_x[qq] += __shfl_xor_sync(0xffffffffu, l_x[qq], 8);
+      l_x[qq] += __shfl_xor_sync(0xffffffffu, l_x[qq], 16);
     }
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      const int xrow = xr0 + g + rr * 8;
+    for (int qq = 0; qq < 2; ++qq) {
+      const int xrow = xr0 + 2 * tq + qq;
       if (!alive || xrow >= a.n_q) continue;
-      if (a.num_splits == 1) {
-        const float inv = l_x[rr] > 0.f ? 1.f / l_x[rr] : 0.f;
-        uint16_t* dst = a.out + ((long long)xrow * H + h) * kHeadDim;
+      const float inv = l_x[qq] > 0.f ? 1.f / l_x[qq] : 0.f;
+      const long long ro = ((long long)split * a.n_q + xrow) * H + h;
 #pragma unroll
-        for (int dt = 0; dt < 8; ++dt)
-          *reinterpret_cast<uint32_t*>(dst + dt * 8 + 2 * tq) =
-              pack_bf16(ox[dt][2 * rr] * inv, ox[dt][2 * rr + 1] * inv);
-      } else {
-        const long long ro = ((long long)split * a.n_q + xrow) * H + h;
-        float* dst = a.part_o + ro * kHeadDim;
+      for (int dt = 0; dt < 4; ++dt)
 #pragma unroll
-        for (int dt = 0; dt < 8; ++dt)
-          *reinterpret_cast<float2*>(dst + dt * 8 + 2 * tq) = make_float2(ox[dt][2 * rr], ox[dt][2 * rr + 1]);
-        if (tq == 0) *reinterpret_cast<float2*>(a.part_ml + ro * 2) = make_float2(m_x[rr], l_x[rr]);
-      }
+        for (int hi = 0; hi < 2; ++hi) {
+          const int d = dt * 16 + g + hi * 8;
+          const float val = ox[dt][2 * hi + qq];
+          if (a.num_splits == 1)
+            a.out[((long long)xrow * H + h) * kHeadDim + d] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(val * inv));
+          else
+            a.part_o[ro * kHeadDim + d] = val;
+        }
+      if (a.num_splits > 1 && g == 0)
+        *reinterpret_cast<float2*>(a.part_ml + ro * 2) = make_float2(m_x[qq], l_x[qq]);
     }
   }
 
@@ -792,7 +792,7 @@ struct TcShape {
   bool extra;
 };
 
-// Query rows per CTA: up to two 128-row M-tiles, plus up to 16 extra rows when
+// Query rows per CTA: up to two 128-row M-tiles, plus up to 8 extra rows when
 // the whole query fits one group that way (a frame's 256 + 6 tokens); longer
 // queries (a chunk's tokens) are cut into groups of 256 rows.
 TcShape tc_shape(int n_q) {
