@@ -20,8 +20,8 @@
 //   warps 4..    one warpgroup per M-tile (a thread per query row): copies its S
 //                row from TMEM to registers (freeing S for the next QK), masks
 //                invalid slots, keeps a running max (only raised when it grows by
-//                more than 2^8, so O rarely needs rescaling), writes P = 2^(S - m)
-//                as bf16 into shared memory and finally reads O from TMEM.
+//                more than 2^64), writes P = 2^(S - m) as bf16 back into TMEM,
+//                where PV takes its A operand, and finally reads O from TMEM.
 //   warp 0       the extra rows (at most 8, if any): the same tiles through
 //                warp-level mma.sync tiles, entirely in registers; an M=128
 //                tensor-core tile for 6 rows would cost as much as a full one.
@@ -38,12 +38,15 @@ namespace pkv {
 namespace {
 
 constexpr int kBN = 128;           // slots per KV tile
-constexpr int kStages = 4;         // KV ring depth
+constexpr int kStages = 6;         // KV ring depth
 constexpr int kXRows = 8;          // extra query rows handled with mma.sync
-// TMEM columns: S_m at 128m, O_m at 128*MT + 64m; the allocation is a power of two.
+// TMEM columns: S_m (fp32) at 128m, O_m (fp32) at 128*MT + 64m, P_m (bf16
+// pairs, 64 columns for 128 slots) at 192*MT + 64m; the allocation is a power
+// of two.
 template <int MT>
 struct TmemCols {
   static constexpr int kO = 128 * MT;
+  static constexpr int kP = 192 * MT;
   static constexpr int kAlloc = MT == 1 ? 256 : 512;
 };
 constexpr uint32_t kSpinLimit = 1u << 25;
@@ -54,7 +57,6 @@ struct __align__(1024) TcSmem {
   uint8_t q[MT][128 * 128];          // Q_m: 128 rows x 64 bf16, 128B-swizzled
   uint8_t k[kStages][kBN * 128];     // K tile: 128 slots x 64 bf16
   uint8_t v[kStages][kBN * 128];
-  uint8_t p[MT][2][128 * 128];       // P_m: two 64-slot atoms of 128 rows x 128 B
   uint64_t mask[kStages][2];         // slot validity of the stage's tile
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
@@ -167,6 +169,14 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
+// Same, with the A operand in TMEM (128 lanes = rows, K packed two bf16 per column).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
@@ -193,6 +203,17 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),           \
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])            \
       : "r"(taddr))
+
+#define PKV_TMEM_ST32(taddr, r)                                                                  \
+  asm volatile(                                                                                  \
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"    \
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::  \
+          "r"(taddr),                                                                            \
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),   \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),         \
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),       \
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),       \
+      "r"(r[29]), "r"(r[30]), "r"(r[31]))
 
 #define PKV_TMEM_ST16(taddr, r)                                                                  \
   asm volatile(                                                                                  \
@@ -406,8 +427,6 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
       constexpr uint32_t kIdQK = idesc_bf16(128, kBN, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, kHeadDim, true);
       const uint64_t qa = sdesc(smem_u32(&sm.q[m][0]));
-      const uint64_t pa0 = sdesc(smem_u32(&sm.p[m][0][0]));
-      const uint64_t pa1 = sdesc(smem_u32(&sm.p[m][1][0]));
       for (int j = 0; j <= nT && nT > 0; ++j) {
         if (j < nT) {
           if (!mbar_wait(&sm.kv_full[j % kStages], (j / kStages) & 1, abort, a.err)) break;
@@ -428,8 +447,9 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
           const uint64_t vb = sdesc(smem_u32(&sm.v[jp % kStages][0]));
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            tc_mma(tmem + TmemCols<MT>::kO + m * kHeadDim, (kk < 4 ? pa0 : pa1) + 2 * (kk & 3),
-                   vb + 128 * kk, kIdPV, (jp > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_ts(tmem + TmemCols<MT>::kO + m * kHeadDim,
+                      tmem + TmemCols<MT>::kP + m * (kBN / 2) + 8 * kk, vb + 128 * kk, kIdPV,
+                      (jp > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&sm.o_done[m]);
           tc_commit(&sm.kv_empty[jp % kStages]);
         }
@@ -448,6 +468,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
     const uint32_t t_s = tmem + t_lane + m * kBN;
     const uint32_t t_o = tmem + t_lane + TmemCols<MT>::kO + m * kHeadDim;
+    const uint32_t t_p = tmem + t_lane + TmemCols<MT>::kP + m * (kBN / 2);
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;          // running max (log2 units) and sum
     bool alive = true;
@@ -576,19 +597,13 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
         }
         tmem_wait_st();
       }
-      // P row (bf16, two 64-slot atoms) into the swizzled P tile
-#pragma unroll
-      for (int at = 0; at < 2; ++at) {
-        uint8_t* p_row = &sm.p[m][at][r * 128];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t* q4 = &pk[at * 32 + 4 * c];
-          *reinterpret_cast<uint4*>(p_row + (swizzle_chunk(r, c) << 4)) =
-              make_uint4(q4[0], q4[1], q4[2], q4[3]);
-        }
+      // P row (bf16 pairs) into TMEM, where PV reads its A operand
+      if (warp_active) {
+        PKV_TMEM_ST32(t_p, pk);
+        PKV_TMEM_ST32(t_p + 32, (&pk[32]));
+        tmem_wait_st();
       }
       // S_m has been read and P_m written: QK(m, j+1) and PV(m, j) may go
-      fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&sm.p_full[m]);
     }
