@@ -50,7 +50,7 @@ struct TmemCols {
   static constexpr int kAlloc = MT == 1 ? 256 : 512;
 };
 constexpr uint32_t kSpinLimit = 1u << 25;
-constexpr float kOverflowGuard = 15.0f;     // log2 units: p stays below 2^15 (f16 range)
+constexpr float kOverflowGuard = 64.0f;     // log2 units: p stays below 2^64
 
 template <int MT>
 struct __align__(1024) TcSmem {
@@ -234,21 +234,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
-}
-
-// Two exponentials at once: x (fp32 pair) is rounded to f16, 2^x comes back as
-// f16 (MUFU handles a packed pair per instruction) and is widened to fp32. The
-// f16 input keeps 11 bits, so |2^x| carries a relative error of at most
-// 2^-11 * ln2 * |x| from that rounding; callers keep x <= 15 (no overflow).
-__device__ __forceinline__ float2 exp2_pair(float x0, float x1) {
-  uint32_t h, e;
-  asm("cvt.rn.f16x2.f32 %0, %2, %1;\n" : "=r"(h) : "f"(x0), "f"(x1));
-  asm("ex2.approx.f16x2 %0, %1;\n" : "=r"(e) : "r"(h));
-  float2 r;
-  asm("{\n .reg .f16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.f32.f16 %0, lo;\n cvt.f32.f16 %1, hi;\n}\n"
-      : "=f"(r.x), "=f"(r.y)
-      : "r"(e));
-  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -504,9 +489,8 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
       // Fast path: exponentiate against the running max of the earlier tiles and
       // track this tile's max on the way, 64 columns at a time. Any reference
       // keeps the result exact (it cancels in O / l); it only has to keep
-      // 2^(s - m) in the f16 range of exp2_pair, so the exact path (tile max
-      // first, O rescaled) runs on the first tile and when the max has grown by
-      // more than 2^15.
+      // 2^(s - m) finite, so the exact path (tile max first, O rescaled) runs on
+      // the first tile and when the max has grown by more than 2^64.
       uint32_t pk[kBN / 2];                        // P row as bf16 pairs
       bool rescale = false;
       float alpha = 1.f;
@@ -531,10 +515,11 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
           for (int c = 0; c < 64; c += 2) {
             t0m = fmaxf(t0m, v[c]);
             t1m = fmaxf(t1m, v[c + 1]);
-            const float2 pp = exp2_pair(fmaf(v[c], sl2, -m_ref), fmaf(v[c + 1], sl2, -m_ref));
-            pk[32 * hf + (c >> 1)] = pack_bf16(pp.x, pp.y);
-            sum0 += pp.x;
-            sum1 += pp.y;
+            const float p0 = fast_exp2(fmaf(v[c], sl2, -m_ref));
+            const float p1 = fast_exp2(fmaf(v[c + 1], sl2, -m_ref));
+            pk[32 * hf + (c >> 1)] = pack_bf16(p0, p1);
+            sum0 += p0;
+            sum1 += p1;
           }
         }
         redo = fmaxf(t0m, t1m) * sl2 > m_ref + kOverflowGuard;
@@ -576,10 +561,11 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
               if (!((bits >> c) & 1ull)) v[c] = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 64; c += 2) {
-              const float2 pp = exp2_pair(fmaf(v[c], sl2, -m_ref), fmaf(v[c + 1], sl2, -m_ref));
-              pk[32 * hf + (c >> 1)] = pack_bf16(pp.x, pp.y);
-              sum0 += pp.x;
-              sum1 += pp.y;
+              const float p0 = fast_exp2(fmaf(v[c], sl2, -m_ref));
+              const float p1 = fast_exp2(fmaf(v[c + 1], sl2, -m_ref));
+              pk[32 * hf + (c >> 1)] = pack_bf16(p0, p1);
+              sum0 += p0;
+              sum1 += p1;
             }
           }
         }
