@@ -191,6 +191,31 @@ pkv_status pkv_attend(pkv_t h, const void* q, int n_q, int stream_id, int layer,
 pkv_status pkv_attend_chunked(pkv_t h, const void* q, int n_q, int stream_id, int layer,
                               void* out, float sm_scale, void* cuda_stream);
 
+/* Attention that allocates nothing (no counterpart in the paper; it serves callers
+ * of this library).
+ * Same inputs, outputs, numerics and errors as pkv_attend (frame-mode streams) and
+ * pkv_attend_chunked (chunked-mode streams, n_q = the open chunk's tokens), but the
+ * split-KV partial results live in one fixed block of device memory compiled into
+ * the library (a file-scope static __device__ array of 16 MiB), instead of the
+ * scratch that pkv_attend grows with cudaMalloc the first time it needs more.
+ * Some callers cannot allocate device memory at call time: code that runs while a
+ * CUDA graph is being captured (an allocation would break the capture), real-time
+ * frame loops that cannot afford the device-wide synchronisation cudaMalloc and
+ * cudaFree imply, and hosts whose device memory belongs to another allocator. They
+ * can create the handle and open the stream up front and then call this.
+ *  - A call whose partial results need more than 16 MiB (num_splits x n_q x heads
+ *    x 264 bytes; e.g. a whole 8 x 1374-token chunk) returns PKV_ERR_INVALID and
+ *    launches nothing.
+ *  - The first call on a device resolves the array's device address
+ *    (cudaGetSymbolAddress) for that device; make that first call before any
+ *    stream capture.
+ *  - Every call, on every handle and stream, shares the one array, which keeps
+ *    the last call's contents (nothing in it needs to start at zero: each call
+ *    writes every partial it reads). Calls that overlap on the GPU race: order
+ *    them on one CUDA stream. */
+pkv_status pkv_attend_noalloc(pkv_t h, const void* q, int n_q, int stream_id, int layer, void* out,
+                              float sm_scale, void* cuda_stream);
+
 /* Wait for `cuda_stream` and report the device error word (PKV_ERR_DEVICE) or a
  * pending CUDA error (PKV_ERR_CUDA). */
 pkv_status pkv_sync(pkv_t h, void* cuda_stream);

@@ -122,6 +122,15 @@ class PagedKVCache:
                                                 _stream_ptr(stream)))
         return out
 
+    def attend_noalloc(self, q, sid, layer=0, out=None, sm_scale=0.0, stream=None):
+        """pkv_attend_noalloc: attention whose scratch is a fixed device array."""
+        if out is None:
+            out = torch.empty_like(q)
+        self._check(self.lib.pkv_attend_noalloc(self.h, _bf16_ptr(q, "q"), q.shape[0], sid, layer,
+                                                _bf16_ptr(out, "out"), float(sm_scale),
+                                                _stream_ptr(stream)))
+        return out
+
     def sync(self, stream=None):
         self._check(self.lib.pkv_sync(self.h, _stream_ptr(stream)))
 

@@ -14,6 +14,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -908,6 +909,98 @@ pkv_status pkv_synth_fill(void* dst, int n_frames, int n_tokens, int heads, int 
   cudaError_t e = launch_synth(static_cast<uint16_t*>(dst), n_frames, n_tokens, heads, head_dim,
                                key_base, frame0, token0, scale, as_stream(cuda_stream));
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "pkv_synth_fill");
+  return PKV_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Attention without allocation: the split-KV partials live in a fixed array.
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;   // 16 MiB
+// The partial (o, m, l) results of pkv_attend_noalloc, shared by every call on
+// every handle. In host code this name is only a stand-in for the symbol: kernels
+// get the device address resolved by cudaGetSymbolAddress below.
+static __device__ __align__(256) float g_noalloc_scratch[kStaticScratchBytes / sizeof(float)];
+
+constexpr int kMaxDevices = 64;
+float* g_noalloc_ptr[kMaxDevices] = {nullptr};
+std::mutex g_noalloc_mu;
+
+// Device address of the static scratch on the current device, resolved once per
+// device (with that device current).
+pkv_status noalloc_scratch(pkv_t h, float** out) {
+  int dev = 0;
+  PKV_CUDA(h, cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return fail(h, PKV_ERR_INVALID, "device %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    PKV_CUDA(h, cudaGetSymbolAddress(&p, g_noalloc_scratch));
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_attend_noalloc(pkv_t h, const void* q, int n_q, int sid, int layer, void* out,
+                              float sm_scale, void* cuda_stream) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  if (!q || !out || !aligned16(q) || !aligned16(out))
+    return fail(h, PKV_ERR_INVALID, "q/out must be 16-byte aligned device pointers");
+  if (n_q < 1 || n_q > (1 << 20)) return fail(h, PKV_ERR_INVALID, "n_q %d out of range", n_q);
+  if (layer < 0 || layer >= h->L) return fail(h, PKV_ERR_INVALID, "layer %d out of range", layer);
+  if (st->cfg.mode == PKV_MODE_CHUNKED) {
+    if (!st->c_open) return fail(h, PKV_ERR_STATE, "no open chunk");
+    const int cur = (st->c_head + st->n_chunks - 1) % st->cfg.sliding_window_num;
+    if (n_q != st->c_len[cur])
+      return fail(h, PKV_ERR_INVALID, "n_q %d != the open chunk's %d tokens", n_q, st->c_len[cur]);
+  }
+  int np, nt, last;
+  visible_counts(h, *st, &np, &nt, &last);
+  if (nt == 0) return fail(h, PKV_ERR_STATE, "nothing is visible");
+  AttendArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = static_cast<const uint16_t*>(q);
+  a.out = static_cast<uint16_t*>(out);
+  a.n_q = n_q;
+  a.heads = h->H;
+  a.pool = h->d_pool + (long long)layer * h->P * h->page_elems;
+  a.page_elems = h->page_elems;
+  a.page_size = h->Ps;
+  a.pool_pages = h->P;
+  a.tbl_idx = st->d_tbl_idx;
+  a.tbl_len = st->d_tbl_len;
+  a.n_entries = np;
+  a.n_slots = (long long)(np - 1) * h->Ps + last;
+  a.n_tiles = ceil_div(a.n_slots, 64);
+  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)h->D);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.num_splits = attend_num_splits(n_q, h->H, a.n_slots, h->num_sms);
+  a.err = h->d_err;
+  if (a.num_splits > 1) {
+    const size_t o_bytes = (size_t)a.num_splits * n_q * h->H * kHeadDim * sizeof(float);
+    const size_t ml_bytes = (size_t)a.num_splits * n_q * h->H * 2 * sizeof(float);
+    if (o_bytes + ml_bytes > kStaticScratchBytes)
+      return fail(h, PKV_ERR_INVALID,
+                  "this call needs %zu bytes of split-KV scratch; the static scratch holds %zu",
+                  o_bytes + ml_bytes, kStaticScratchBytes);
+    float* scratch = nullptr;
+    if (pkv_status r = noalloc_scratch(h, &scratch)) return r;
+    a.part_o = scratch;
+    a.part_ml = scratch + o_bytes / sizeof(float);
+  }
+  cudaStream_t s = as_stream(cuda_stream);
+  TableArgs t = table_args(h, *st, st->d_tbl_idx, st->d_tbl_len, nullptr, nullptr);
+  PKV_CUDA(h, launch_table(t, s));
+  PKV_CUDA(h, launch_attend(a, h->num_sms, s));
   return PKV_OK;
 }
 
