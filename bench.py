@@ -48,6 +48,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--profile-frames", type=int, default=0,
                    help="run N frames of the stream once, eagerly, and exit (a small case for ncu)")
+    p.add_argument("--profile-chunks", type=int, default=0,
+                   help="run N chunks of the chunked workload once and exit (a small case for ncu)")
+    p.add_argument("--no-extra", action="store_true", help="skip the extra workload measurements")
     return p.parse_args()
 
 
@@ -171,11 +174,13 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def attend_traffic_per_launch():
-    """DRAM bytes per attend launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
+def attend_traffic_per_launch(avg_visible_tokens):
+    """DRAM bytes of one attention launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None), scaled from the captured
+    frame's visible tokens to the stream's average (traffic is proportional to the
+    visible K/V bytes). The capture is cold-cache (ncu flushes between passes)."""
     path = os.path.join(ROOT, "profiles", "attend_lingbot_ncu.md")
-    src = os.path.join(ROOT, "paged_kv_cache_build_gb300", "csrc", "pkv_attend.cu")
+    src = os.path.join(ROOT, "paged_kv_cache_build_gb300", "csrc", "pkv_attend_tc.cu")
     if not os.path.exists(path):
         return None
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
@@ -183,12 +188,12 @@ def attend_traffic_per_launch():
     for line in open(path):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
-            vals[k.strip()] = v.strip()
+            vals[k.strip()] = v.strip().split()[0]
     if vals.get("kernel_source_sha256_16") != digest:
         return None
     try:
-        return float(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
+        return float(vals["dram_bytes_per_launch"]) * avg_visible_tokens / float(vals["captured_visible_tokens"])
+    except (KeyError, ValueError, ZeroDivisionError):
         return None
 
 
@@ -257,6 +262,136 @@ def oracle_sample(w, seconds, rank_tag=0):
             "sample": f"fp64 numpy oracle: metadata state machine over all 512 frames (untimed), then "
                       f"gather + softmax attention of steady-state frame {t_last} (21,504 visible "
                       f"tokens, 262 queries, 16 heads) repeated {n_frames}x in {el:.1f} s"}
+
+
+# ------------------------------------------------------- extra workloads
+def _events():
+    import torch
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def extra_chunked(reps=5):
+    """VGGT-style chunked attention at steady state: 4 visible chunks (43,968 slots),
+    the current chunk's 10,992 queries, 16 heads x 64: attention TFLOP/s."""
+    import torch
+    from paged_kv_cache_build_gb300 import PagedKVCache, chunked_stream_cfg, synth_fill
+    from synth import TENSOR_K, TENSOR_Q, TENSOR_V, WORKLOADS
+    w = WORKLOADS["chunked"]
+    cache = PagedKVCache(w.pool_pages, w.page_size, w.heads, w.head_dim)
+    sid = cache.open_stream(chunked_stream_cfg(w.chunk_size, w.sliding_window_num, w.tokens_per_frame))
+    n_fr = w.chunk_size * w.sliding_window_num
+    k = torch.empty((n_fr, w.tokens_per_frame, w.heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    synth_fill(k, 0, w.index, sid, 0, 0, TENSOR_K)
+    synth_fill(v, 0, w.index, sid, 0, 0, TENSOR_V)
+    for f in range(n_fr):
+        cache.append_frame(sid, k[f], v[f])
+        if f % w.chunk_size == w.chunk_size - 1 and f < n_fr - 1:
+            cache.evict_window(sid)
+    n_q = w.chunk_size * w.tokens_per_frame
+    q = torch.empty((n_q, w.heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    synth_fill(q, 0, w.index, sid, 0, n_fr - w.chunk_size, TENSOR_Q, 0)
+    out = torch.empty_like(q)
+    for _ in range(2):
+        cache.attend_chunked(q, sid, out=out, sm_scale=w.sm_scale)
+    torch.cuda.synchronize()
+    e0, e1 = _events()
+    e0.record()
+    for _ in range(reps):
+        cache.attend_chunked(q, sid, out=out, sm_scale=w.sm_scale)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    n_kv = cache.visible_count(sid)[1]
+    flops = 4.0 * n_q * n_kv * w.head_dim * w.heads
+    cache.sync()
+    cache.close()
+    return {"workload": "vggt-chunked-8x1374-W4-16x64", "n_q": n_q, "visible_slots": n_kv,
+            "ms_per_chunk": round(ms, 4), "attn_tflops": round(flops / (ms * 1e-3) / 1e12, 2)}
+
+
+def extra_long24(frames=240, warm=100):
+    """The 24-layer keyframe stream (kf 4): per frame, for each layer, append and
+    attend; then evict (keyframe) or roll back. frame-steps/s over `frames` frames
+    after `warm` frames (inputs from a ring of 8 frames per layer)."""
+    import torch
+    from paged_kv_cache_build_gb300 import PagedKVCache, frame_stream_cfg, synth_fill
+    from synth import TENSOR_K, TENSOR_Q, TENSOR_V, WORKLOADS, is_keyframe
+    w = WORKLOADS["long"]
+    L, R = w.layers, 8
+    cache = PagedKVCache(w.pool_pages, w.page_size, w.heads, w.head_dim, layers=L)
+    sid = cache.open_stream(frame_stream_cfg(w.num_scale, w.window, w.n_patch, w.n_special))
+    shape = (L, R, w.frame_tokens, w.heads, w.head_dim)
+    k = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    v, q = torch.empty_like(k), torch.empty_like(k)
+    out = torch.empty((w.frame_tokens, w.heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    for layer in range(L):
+        synth_fill(k[layer], 0, w.index, sid, layer, 0, TENSOR_K)
+        synth_fill(v[layer], 0, w.index, sid, layer, 0, TENSOR_V)
+        synth_fill(q[layer], 0, w.index, sid, layer, 0, TENSOR_Q, 0, w.q_scale)
+
+    def frame(t):
+        for layer in range(L):
+            cache.append_frame(sid, k[layer, t % R], v[layer, t % R], layer)
+            cache.attend(q[layer, t % R], sid, layer, out=out, sm_scale=w.sm_scale)
+        if is_keyframe(t, w.num_scale, w.keyframe_interval):
+            cache.evict_window(sid)
+        else:
+            cache.rollback_last_frame(sid)
+
+    for t in range(warm):
+        frame(t)
+    torch.cuda.synchronize()
+    e0, e1 = _events()
+    e0.record()
+    for t in range(warm, warm + frames):
+        frame(t)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    cache.sync()
+    cache.close()
+    return {"workload": "long-24layer-kf4 (frames %d-%d, eager calls)" % (warm, warm + frames - 1),
+            "frame_steps_per_s": round(frames / (ms * 1e-3), 2),
+            "ms_per_frame_step": round(ms / frames, 4)}
+
+
+def extra_append(reps=20):
+    """32 streams' frames appended in one batched launch (pkv_append_frames):
+    2 x 262 x 16 x 64 x 2 B read and written per stream: GB/s against HBM."""
+    import torch
+    from paged_kv_cache_build_gb300 import PagedKVCache, frame_stream_cfg, synth_fill
+    from synth import TENSOR_K, TENSOR_V, WORKLOADS
+    w = WORKLOADS["multistream"]
+    n = w.streams
+    cache = PagedKVCache(w.pool_pages, w.page_size, w.heads, w.head_dim, max_streams=64)
+    sids = [cache.open_stream(frame_stream_cfg(w.num_scale, w.window, w.n_patch, w.n_special))
+            for _ in range(n)]
+    kv = torch.empty((2, n, w.frame_tokens, w.heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    synth_fill(kv[0], 0, w.index, 0, 0, 0, TENSOR_K)
+    synth_fill(kv[1], 0, w.index, 0, 0, 0, TENSOR_V)
+    ks, vs = [kv[0, i] for i in range(n)], [kv[1, i] for i in range(n)]
+    times = []
+    for r in range(reps + 3):
+        e0, e1 = _events()
+        e0.record()
+        cache.append_frames(sids, ks, vs)
+        e1.record()
+        for s in sids:
+            cache.evict_window(s)
+        torch.cuda.synchronize()
+        if r >= 3:
+            times.append(e0.elapsed_time(e1))
+    cache.sync()
+    cache.close()
+    ms = statistics.median(times)
+    moved = 2.0 * 2 * n * w.frame_tokens * w.heads * w.head_dim * 2
+    peaks, kind = measured_peaks()
+    gbs = moved / (ms * 1e-3) / 1e9
+    return {"workload": "32-stream batched append, 256+6 tokens x 16 x 64 bf16",
+            "bytes_per_launch": int(moved), "us_per_launch": round(ms * 1e3, 2),
+            "gbs": round(gbs, 1), "hbm_peak_gbs": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 3),
+            "peak_source": kind}
 
 
 # ------------------------------------------------------------- our arm
@@ -427,7 +562,8 @@ def run_ours(args):
         "attn_us_per_frame": round(att_ms * 1e3 / (F * n_att_steps), 3),
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(attn_tflops / peak, 4),
-                     "traffic": attend_traffic_per_launch(),
+                     "traffic": attend_traffic_per_launch(
+                         sum(visible_tokens(w, t) for t in range(F)) / F),
                      "peak_source": f"bf16_tflops_sustained ({peak_kind}); kernel: pkv_attend call "
                                     f"(table + attention + split combine), useful flops "
                                     f"4*262*N_kv*64*16 per frame, every frame of the stream"},
@@ -438,6 +574,8 @@ def run_ours(args):
         "launches_per_step": int(per_step_launches),
         "clocks": clocks.summary(),
     }
+    if not args.no_extra:
+        line["extra"] = {"chunked": extra_chunked(), "long24": extra_long24(), "append": extra_append()}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -524,9 +662,37 @@ def run_profile(args):
     print(json.dumps({"profile_frames": n, "visible": cache.visible_count(sid)}))
 
 
+def run_profile_chunked(args):
+    """N chunks of the chunked workload, eagerly: one chunked attend per chunk."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_cache_build_gb300 import PagedKVCache, chunked_stream_cfg, synth_fill
+    from synth import TENSOR_K, TENSOR_Q, TENSOR_V, WORKLOADS
+    w = WORKLOADS["chunked"]
+    cache = PagedKVCache(w.pool_pages, w.page_size, w.heads, w.head_dim)
+    sid = cache.open_stream(chunked_stream_cfg(w.chunk_size, w.sliding_window_num, w.tokens_per_frame))
+    k = torch.empty((w.chunk_size, w.tokens_per_frame, w.heads, w.head_dim), dtype=torch.bfloat16,
+                    device="cuda")
+    v, q = torch.empty_like(k), torch.empty_like(k)
+    for c in range(args.profile_chunks):
+        synth_fill(k, 0, w.index, sid, 0, c * w.chunk_size, TENSOR_K)
+        synth_fill(v, 0, w.index, sid, 0, c * w.chunk_size, TENSOR_V)
+        synth_fill(q, 0, w.index, sid, 0, c * w.chunk_size, TENSOR_Q)
+        for f in range(w.chunk_size):
+            cache.append_frame(sid, k[f], v[f])
+        cache.attend_chunked(q.view(-1, w.heads, w.head_dim), sid, sm_scale=w.sm_scale)
+        cache.evict_window(sid)
+    torch.cuda.synchronize()
+    cache.sync()
+    print(json.dumps({"profile_chunks": args.profile_chunks}))
+
+
 def main():
     args = parse()
-    if args.profile_frames:
+    if args.profile_chunks:
+        run_profile_chunked(args)
+    elif args.profile_frames:
         run_profile(args)
     elif args.impl == "reference":
         run_reference(args)
