@@ -13,7 +13,7 @@ from oracle import PagedCacheOracle, StreamConfig, attend_fp64, gather_visible
 from synth import TENSOR_K, TENSOR_Q, TENSOR_V, frame_tensor
 from synth.inputs import bf16_bits_to_f64
 
-# Spec tolerance for bf16 inputs against the fp64 oracle.
+# Required agreement of bf16 inputs with the fp64 oracle (max and mean absolute error).
 MAX_ABS = 2e-2
 MEAN_ABS = 2e-3
 
@@ -125,7 +125,7 @@ class Pair:
 
 
 def assert_close(gpu_out, oracle_out, e_abs_v, what=""):
-    """Spec tolerance, plus the bound derived from the arithmetic: bf16
+    """The required max/mean tolerance, plus the bound derived from the arithmetic: bf16
     output rounding (2^-9 |o|) and bf16 rounding of the softmax weights
     (2^-9 E_p|v|), with a factor 2 margin and fp32 slack."""
     g = bf16_bits_to_f64(gpu_out.view(torch.int16).cpu().numpy().view(np.uint16))

@@ -1,7 +1,7 @@
 """Parity of the CUDA library with the CPU oracle (needs a GB300).
 
 Page tables, free stacks and slot contents must match bit for bit; attention
-outputs must be within the benchmark spec's tolerance (max abs 2e-2, mean abs 2e-3
+outputs must be within the required tolerance (max abs 2e-2, mean abs 2e-3
 against fp64) and within the bound derived from bf16 rounding (see
 tests/pairing.py)."""
 
