@@ -279,7 +279,9 @@ __device__ __forceinline__ void tile_mask(const AttendArgs& a, int tile, uint64_
     const int f0 = tile * kBN + pp * rows;
     const int e = f0 / Ps, so = f0 - e * Ps;
     if (e >= a.n_entries) break;
-    int n = __ldg(&a.tbl_len[e]) - so;
+    int page, len;
+    table_entry(a.tbl, e, page, len);
+    int n = len - so;
     n = n < 0 ? 0 : (n > rows ? rows : n);
     const int b0 = pp * rows;                    // first bit of this block
     // set bits [b0, b0 + n)
@@ -383,7 +385,8 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
           const int f0 = tile * kBN + pp * rows;
           const int e = f0 / Ps, so = f0 - e * Ps;
           if (e >= a.n_entries) break;
-          int page = __ldg(&a.tbl_idx[e]);
+          int page, len;
+          table_entry(a.tbl, e, page, len);
           if (page < 0 || page >= a.pool_pages) {
             atomicOr(a.err, kErrPageRange);
             page = 0;

@@ -748,8 +748,6 @@ static pkv_status attend_common(pkv_t h, Stream* st, const void* q, int n_q, int
   int np, nt, last;
   visible_counts(h, *st, &np, &nt, &last);
   if (nt == 0) return fail(h, PKV_ERR_STATE, "nothing is visible");
-  TableArgs t = table_args(h, *st, st->d_tbl_idx, st->d_tbl_len, nullptr, nullptr);
-  PKV_CUDA(h, launch_table(t, s));
   AttendArgs a;
   std::memset(&a, 0, sizeof(a));
   a.q = static_cast<const uint16_t*>(q);
@@ -762,6 +760,7 @@ static pkv_status attend_common(pkv_t h, Stream* st, const void* q, int n_q, int
   a.pool_pages = h->P;
   a.tbl_idx = st->d_tbl_idx;
   a.tbl_len = st->d_tbl_len;
+  a.tbl = table_args(h, *st, st->d_tbl_idx, st->d_tbl_len, nullptr, nullptr);
   a.n_entries = np;
   a.n_slots = (long long)(np - 1) * h->Ps + last;
   a.n_tiles = ceil_div(a.n_slots, 64);
@@ -978,6 +977,7 @@ pkv_status pkv_attend_noalloc(pkv_t h, const void* q, int n_q, int sid, int laye
   a.pool_pages = h->P;
   a.tbl_idx = st->d_tbl_idx;
   a.tbl_len = st->d_tbl_len;
+  a.tbl = table_args(h, *st, st->d_tbl_idx, st->d_tbl_len, nullptr, nullptr);
   a.n_entries = np;
   a.n_slots = (long long)(np - 1) * h->Ps + last;
   a.n_tiles = ceil_div(a.n_slots, 64);
@@ -998,8 +998,6 @@ pkv_status pkv_attend_noalloc(pkv_t h, const void* q, int n_q, int sid, int laye
     a.part_ml = scratch + o_bytes / sizeof(float);
   }
   cudaStream_t s = as_stream(cuda_stream);
-  TableArgs t = table_args(h, *st, st->d_tbl_idx, st->d_tbl_len, nullptr, nullptr);
-  PKV_CUDA(h, launch_table(t, s));
   PKV_CUDA(h, launch_attend(a, h->num_sms, s));
   return PKV_OK;
 }

@@ -150,6 +150,33 @@ struct TableArgs {
   int* err;
 };
 
+// Entry e of a stream's visible table (page id, valid slots): scale pages, window
+// pages oldest first, special pages (frame mode); chunks oldest first (chunked).
+__device__ __forceinline__ void table_entry(const TableArgs& t, int e, int& id, int& len) {
+  if (t.mode == 0) {
+    if (e < t.n_scale) {
+      id = t.scale[e];
+      len = t.page_size;
+    } else if (e < t.n_scale + t.win_count) {
+      id = t.window[(t.win_head + e - t.n_scale) % t.win_cap];
+      len = t.page_size;
+    } else {
+      const int k = e - t.n_scale - t.win_count;
+      id = t.special[k];
+      len = (k == t.n_special - 1) ? t.sp_last_len : t.sp_full_len;
+    }
+  } else {
+    int c = 0, base = 0;
+    while (c < t.n_chunks - 1 && e >= base + t.chunk_npages[c]) {
+      base += t.chunk_npages[c];
+      ++c;
+    }
+    const int k = e - base;
+    id = t.chunk_pages[c][k];
+    len = min(t.page_size, t.chunk_len[c] - k * t.page_size);
+  }
+}
+
 // ---------------------------------------------------------------- attend
 struct AttendArgs {
   const uint16_t* q;                // [n_q][heads][64]
@@ -160,8 +187,9 @@ struct AttendArgs {
   long long page_elems;
   int page_size;
   int pool_pages;
-  const int32_t* tbl_idx;
+  const int32_t* tbl_idx;            // visible table (read by the mma.sync kernel)
   const int32_t* tbl_len;
+  TableArgs tbl;                     // the same table, computed on the fly by the producer
   int n_entries;
   int n_tiles;                      // 64-slot tiles covering the table's slots
   long long n_slots;                // flat slots up to the last valid one

@@ -30,11 +30,12 @@ __device__ __forceinline__ uint16_t* row_ptr(const PoolView& pv, int page, int k
          ((long long)(kv * pv.heads + head) * pv.page_size + slot) * kHeadDim;
 }
 
-// One batched frame-mode append. blockIdx.y selects the stream; every block
-// recomputes that stream's place on the free stack with an exclusive warp scan
-// of the batch's page needs (1, or 2 when the frame opens a special page), so
-// stream i pops after streams 0..i-1 exactly as sequential appends would.
-__global__ void __launch_bounds__(256) frame_append_kernel(const FrameAppendArgs a) {
+// One batched frame-mode append. blockIdx.y selects the stream, blockIdx.x the
+// token; thread (kv, head, 16-byte chunk) moves one vector. Every block
+// recomputes its stream's place on the free stack with an exclusive warp scan of
+// the batch's page needs (1, or 2 when the frame opens a special page), so stream
+// i pops after streams 0..i-1 exactly as sequential appends would.
+__global__ void __launch_bounds__(512) frame_append_kernel(const FrameAppendArgs a) {
   const int b = blockIdx.y;
   __shared__ int s_patch, s_sp;
   if (threadIdx.x < 32) {
@@ -75,67 +76,63 @@ __global__ void __launch_bounds__(256) frame_append_kernel(const FrameAppendArgs
 
   const AppendItem& it = a.item[b];
   const int H = a.pool.heads;
-  const int n_tok = a.n_patch + a.n_special;
-  // A freshly opened special page gets its unused slots zeroed, so that every
-  // slot of a held page is a token or zero.
-  const int zero_slots = it.new_sp ? a.pool.page_size - a.n_special : 0;
-  const long long per_tok = 2LL * H * kChunksPerRow;
-  const long long total = (long long)(n_tok + zero_slots) * per_tok;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const int c = (int)(i & 7);
-    long long r = i >> 3;
-    const int h = (int)(r % H);
-    r /= H;
-    const int kv = (int)(r & 1);
-    const int t = (int)(r >> 1);
-    uint4 val;
-    int page, slot;
-    if (t < n_tok) {
-      const uint16_t* src = (kv ? it.v : it.k) + ((long long)t * H + h) * kHeadDim + c * 8;
-      val = __ldg(reinterpret_cast<const uint4*>(src));
-      if (t < a.n_patch) {
-        page = patch;
-        slot = t;
-      } else {
-        page = sp;
-        slot = it.sp_off + (t - a.n_patch);
-      }
-    } else {
-      val = make_uint4(0u, 0u, 0u, 0u);
-      page = sp;
-      slot = a.n_special + (t - n_tok);
-    }
-    uint16_t* dst = row_ptr(a.pool, page, kv, h, slot) + swizzle_chunk(slot, c) * 8;
-    *reinterpret_cast<uint4*>(dst) = val;
+  const int hh = threadIdx.x >> 3, c = threadIdx.x & 7;
+  if (hh >= 2 * H) return;                   // blocks have at least one full warp
+  const int kv = hh >= H ? 1 : 0;
+  const int h = hh - kv * H;
+  const int t = blockIdx.x;
+  // token t of the frame
+  {
+    const uint16_t* src = (kv ? it.v : it.k) + ((long long)t * H + h) * kHeadDim + c * 8;
+    const uint4 val = __ldg(reinterpret_cast<const uint4*>(src));
+    const int page = t < a.n_patch ? patch : sp;
+    const int slot = t < a.n_patch ? t : it.sp_off + (t - a.n_patch);
+    *reinterpret_cast<uint4*>(row_ptr(a.pool, page, kv, h, slot) + swizzle_chunk(slot, c) * 8) = val;
+  }
+  // a freshly opened special page gets its unused slots zeroed, so that every
+  // slot of a held page is a token or zero
+  if (it.new_sp && t < a.pool.page_size - a.n_special) {
+    const int slot = a.n_special + t;
+    *reinterpret_cast<uint4*>(row_ptr(a.pool, sp, kv, h, slot) + swizzle_chunk(slot, c) * 8) =
+        make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
 // Chunked-mode append: the frame's tokens are packed after the chunk's pos0
-// tokens; pages of the chunk past old_pages are popped by this append.
-__global__ void __launch_bounds__(256) chunk_append_kernel(const ChunkAppendArgs a) {
+// tokens; pages of the chunk past old_pages are popped by this append. One block
+// per token, as above; the first blocks also zero the tail of a freshly popped
+// last page.
+__global__ void __launch_bounds__(512) chunk_append_kernel(const ChunkAppendArgs a) {
   const int Ps = a.pool.page_size;
-  if (a.is_meta && blockIdx.x == 0 && threadIdx.x < a.n_new) {
-    const int p = a.free_stack[a.top - 1 - threadIdx.x];
-    if (page_ok(p, a.pool.pool_pages)) a.chunk_pages[a.old_pages + threadIdx.x] = p;
-    else atomicOr(a.err, kErrPageRange);
+  if (a.is_meta && blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < a.n_new; i += blockDim.x) {
+      const int p = a.free_stack[a.top - 1 - i];
+      if (page_ok(p, a.pool.pool_pages)) a.chunk_pages[a.old_pages + i] = p;
+      else atomicOr(a.err, kErrPageRange);
+    }
   }
   const int end = a.pos0 + a.n_tokens;
   const int last_pi = (end - 1) / Ps;
-  // zero the tail of a freshly popped last page
   const int zero_slots = (last_pi >= a.old_pages && (end % Ps) != 0) ? Ps - (end % Ps) : 0;
   const int H = a.pool.heads;
-  const long long per_tok = 2LL * H * kChunksPerRow;
-  const long long total = (long long)(a.n_tokens + zero_slots) * per_tok;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const int c = (int)(i & 7);
-    long long r = i >> 3;
-    const int h = (int)(r % H);
-    r /= H;
-    const int kv = (int)(r & 1);
-    const int t = (int)(r >> 1);
-    const int pos = a.pos0 + t;
+  const int hh = threadIdx.x >> 3, c = threadIdx.x & 7;
+  if (hh >= 2 * H) return;
+  const int kv = hh >= H ? 1 : 0;
+  const int h = hh - kv * H;
+  const int t = blockIdx.x;
+  // pass 0: token t; passes 1..: tail slots t, t + gridDim.x, ...
+  for (int pass = 0;; ++pass) {
+    int pos;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (pass == 0) {
+      pos = a.pos0 + t;
+      const uint16_t* src = (kv ? a.v : a.k) + ((long long)t * H + h) * kHeadDim + c * 8;
+      val = __ldg(reinterpret_cast<const uint4*>(src));
+    } else {
+      const int z = t + (pass - 1) * (int)gridDim.x;
+      if (z >= zero_slots) break;
+      pos = end + z;
+    }
     const int pi = pos / Ps;
     const int slot = pos - pi * Ps;
     const int page = (pi < a.old_pages || !a.is_meta)
@@ -145,13 +142,7 @@ __global__ void __launch_bounds__(256) chunk_append_kernel(const ChunkAppendArgs
       atomicOr(a.err, kErrPageRange);
       continue;
     }
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (t < a.n_tokens) {
-      const uint16_t* src = (kv ? a.v : a.k) + ((long long)t * H + h) * kHeadDim + c * 8;
-      val = __ldg(reinterpret_cast<const uint4*>(src));
-    }
-    uint16_t* dst = row_ptr(a.pool, page, kv, h, slot) + swizzle_chunk(slot, c) * 8;
-    *reinterpret_cast<uint4*>(dst) = val;
+    *reinterpret_cast<uint4*>(row_ptr(a.pool, page, kv, h, slot) + swizzle_chunk(slot, c) * 8) = val;
   }
 }
 
@@ -269,28 +260,7 @@ __global__ void __launch_bounds__(256) reset_meta_kernel(const ResetMetaArgs a) 
 __global__ void __launch_bounds__(256) table_kernel(const TableArgs a) {
   for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < a.n; e += gridDim.x * blockDim.x) {
     int id, len;
-    if (a.mode == 0) {
-      if (e < a.n_scale) {
-        id = a.scale[e];
-        len = a.page_size;
-      } else if (e < a.n_scale + a.win_count) {
-        id = a.window[(a.win_head + e - a.n_scale) % a.win_cap];
-        len = a.page_size;
-      } else {
-        const int k = e - a.n_scale - a.win_count;
-        id = a.special[k];
-        len = (k == a.n_special - 1) ? a.sp_last_len : a.sp_full_len;
-      }
-    } else {
-      int c = 0, base = 0;
-      while (c < a.n_chunks - 1 && e >= base + a.chunk_npages[c]) {
-        base += a.chunk_npages[c];
-        ++c;
-      }
-      const int k = e - base;
-      id = a.chunk_pages[c][k];
-      len = min(a.page_size, a.chunk_len[c] - k * a.page_size);
-    }
+    table_entry(a, e, id, len);
     if (!page_ok(id, a.pool_pages)) {
       atomicOr(a.err, kErrPageRange);
       id = 0;
@@ -323,16 +293,14 @@ unsigned long long launch_count() { return g_launches.load(); }
 void count_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
 
 cudaError_t launch_frame_append(const FrameAppendArgs& a, cudaStream_t s) {
-  const long long per_stream = (long long)(a.n_patch + a.pool.page_size) * 2 * a.pool.heads * 8;
-  dim3 grid(blocks_for(per_stream, 256 * 4, 1024), a.n);
-  frame_append_kernel<<<grid, 256, 0, s>>>(a);
+  dim3 grid(a.n_patch + a.n_special, a.n);
+  frame_append_kernel<<<grid, 16 * a.pool.heads < 32 ? 32 : 16 * a.pool.heads, 0, s>>>(a);
   count_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_append(const ChunkAppendArgs& a, cudaStream_t s) {
-  const long long work = (long long)(a.n_tokens + a.pool.page_size) * 2 * a.pool.heads * 8;
-  chunk_append_kernel<<<blocks_for(work, 256 * 4, 2048), 256, 0, s>>>(a);
+  chunk_append_kernel<<<a.n_tokens, 16 * a.pool.heads < 32 ? 32 : 16 * a.pool.heads, 0, s>>>(a);
   count_launches(1);
   return cudaGetLastError();
 }
