@@ -7,28 +7,31 @@
 // the in-window chunks the same way.
 //
 // One CTA computes, for one head, MT (1 or 2) M-tiles of 128 query rows, plus
-// up to 16 extra rows, against a range of 128-slot KV tiles of the visible
-// table (split-KV partials are merged by the combine kernel). A frame's 262
-// tokens are two M-tiles plus 6 extra rows. Roles:
+// up to 8 extra rows, against a range of 64-slot KV tiles of the visible table
+// (split-KV partials are merged by the combine kernel). A frame's 262 tokens
+// are two M-tiles plus 6 extra rows. Roles:
 //   warp 2       producer: one 1-D bulk copy (cp.async.bulk) per page block of a
-//                tile into a 4-stage shared-memory ring, plus the tile's 128-bit
+//                tile into an 8-stage shared-memory ring, plus the tile's 64-bit
 //                slot-validity mask. Pages are stored in the pool already
 //                128-byte swizzled, so a block lands in shared memory as a ready
 //                tensor-core operand; no tensor map is needed.
 //   warps 3, 1   MMA issuers (one thread each, one per M-tile): S_m = Q_m K^T
-//                (N = 128 slots) and O_m += P_m V into TMEM.
-//   warps 4..    one warpgroup per M-tile (a thread per query row): copies its S
-//                row from TMEM to registers (freeing S for the next QK), masks
-//                invalid slots, keeps a running max (only raised when it grows by
-//                more than 2^64), writes P = 2^(S - m) as bf16 back into TMEM,
-//                where PV takes its A operand, and finally reads O from TMEM.
-//   warp 0       the extra rows (at most 8, if any): the same tiles through
-//                warp-level mma.sync tiles, entirely in registers; an M=128
-//                tensor-core tile for 6 rows would cost as much as a full one.
-// The tensor cores take about as long for a 128x64x16 MMA as for a 128x128x16
-// one, so QK runs on 128-slot tiles (N = 128) to halve its instruction count.
-// Every mbarrier wait is bounded; a wait that gives up sets the device error
-// word, and the CTA drains its copies and MMAs and frees TMEM before returning.
+//                (N = 64 slots) into one of two TMEM buffers, and O_m += P_m V
+//                with P_m read from TMEM.
+//   warps 4..    one warpgroup per M-tile (a thread per query row): reads its S
+//                row from TMEM, masks invalid slots, keeps a running max (only
+//                raised when it grows by more than 2^64), and writes P = 2^(S - m)
+//                as bf16 over the S buffer it came from, where PV takes its A
+//                operand; at the end it reads O from TMEM.
+//   warps 0, 4+4MT..  the extra rows (at most 8, if any), one 16-slot quarter of
+//                every tile per warp, through warp-level mma.sync tiles held in
+//                registers; an M = 128 tensor-core tile for 6 rows would cost as
+//                much as a full one.
+// With two S buffers per M-tile, QK of tile j+1 runs while the softmax works on
+// tile j, and PV of tile j while the softmax works on tile j+1; the softmax
+// (its exponentials) sets the pace. Every mbarrier wait is bounded; a wait that
+// gives up sets the device error word, and the CTA drains its copies and MMAs
+// and frees TMEM before returning.
 #include <cuda_bf16.h>
 
 #include "pkv_internal.cuh"
@@ -37,16 +40,16 @@ namespace pkv {
 
 namespace {
 
-constexpr int kBN = 128;           // slots per KV tile
-constexpr int kStages = 6;         // KV ring depth
+constexpr int kBN = 64;            // slots per KV tile
+constexpr int kStages = 8;         // KV ring depth
 constexpr int kXRows = 8;          // extra query rows handled with mma.sync
-// TMEM columns: S_m (fp32) at 128m, O_m (fp32) at 128*MT + 64m, P_m (bf16
-// pairs, 64 columns for 128 slots) at 192*MT + 64m; the allocation is a power
-// of two.
+constexpr int kXWarps = kBN / 16;  // extra-row warps: one 16-slot quarter of a tile each
+// TMEM columns (fp32): S_m buffer b at 64 (2m + b) (P_m of that tile overwrites
+// its first 32 columns as bf16 pairs), O_m at 128 MT + 64m; the allocation is a
+// power of two.
 template <int MT>
 struct TmemCols {
   static constexpr int kO = 128 * MT;
-  static constexpr int kP = 192 * MT;
   static constexpr int kAlloc = MT == 1 ? 256 : 512;
 };
 constexpr uint32_t kSpinLimit = 1u << 25;
@@ -55,15 +58,18 @@ constexpr float kOverflowGuard = 64.0f;     // log2 units: p stays below 2^64
 template <int MT>
 struct __align__(1024) TcSmem {
   uint8_t q[MT][128 * 128];          // Q_m: 128 rows x 64 bf16, 128B-swizzled
-  uint8_t k[kStages][kBN * 128];     // K tile: 128 slots x 64 bf16
+  uint8_t k[kStages][kBN * 128];     // K tile: 64 slots x 64 bf16
   uint8_t v[kStages][kBN * 128];
-  uint64_t mask[kStages][2];         // slot validity of the stage's tile
+  float xo[kXWarps][kXRows][kHeadDim];  // extra rows: each warp's partial O ...
+  float xml[kXWarps][kXRows][2];        // ... and its running max and sum
+  uint64_t mask[kStages];            // slot validity of the stage's tile
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
-  uint64_t s_full[MT];
-  uint64_t p_full[MT];
-  uint64_t o_done[MT];
+  uint64_t s_full[MT][2];            // S_m of the buffer's latest tile is in TMEM
+  uint64_t p_full[MT];               // P_m of the latest tile is in TMEM (O_m rescaled)
+  uint64_t o_done[MT];               // PV of the latest tile has completed
   uint64_t mma_done[MT];
+  uint64_t x_done;                   // the extra-row warps have published their partials
   uint32_t tmem_base;
   int abort;
 };
@@ -83,17 +89,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(addr), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Non-blocking probe of a phase.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -267,37 +262,12 @@ __device__ __forceinline__ uint32_t sw_addr(uint32_t base, int r, int c) {
   return base + r * 128 + (swizzle_chunk(r, c) << 4);
 }
 
-// Slot-validity mask of a 128-slot tile: slot f = 128*tile + c is valid when its
-// table entry exists and the slot is below that page's length.
-__device__ __forceinline__ void tile_mask(const AttendArgs& a, int tile, uint64_t& lo,
-                                          uint64_t& hi) {
-  const int Ps = a.page_size;
-  lo = hi = 0;
-  const int per = Ps >= kBN ? 1 : kBN / Ps;
-  const int rows = Ps >= kBN ? kBN : Ps;
-  for (int pp = 0; pp < per; ++pp) {
-    const int f0 = tile * kBN + pp * rows;
-    const int e = f0 / Ps, so = f0 - e * Ps;
-    if (e >= a.n_entries) break;
-    int page, len;
-    table_entry(a.tbl, e, page, len);
-    int n = len - so;
-    n = n < 0 ? 0 : (n > rows ? rows : n);
-    const int b0 = pp * rows;                    // first bit of this block
-    // set bits [b0, b0 + n)
-    for (int half = 0; half < 2; ++half) {
-      const int lo_bit = max(b0, half * 64), hi_bit = min(b0 + n, half * 64 + 64);
-      if (hi_bit <= lo_bit) continue;
-      const int cnt = hi_bit - lo_bit;
-      const uint64_t bits = (cnt == 64 ? ~0ull : ((1ull << cnt) - 1ull)) << (lo_bit - half * 64);
-      if (half) hi |= bits;
-      else lo |= bits;
-    }
-  }
-}
-
+// Warps: 0 extra rows, 1 MMA issuer (M-tile 1), 2 producer, 3 MMA issuer
+// (M-tile 0), 4 .. 4 + 4 MT - 1 softmax, then kXWarps - 1 more extra-row warps.
 template <int MT, bool EXTRA>
-constexpr int tc_threads() { return (4 + 4 * MT) * 32; }
+__host__ __device__ constexpr int tc_threads() {
+  return (4 + 4 * MT + (EXTRA ? kXWarps - 1 : 0)) * 32;
+}
 constexpr int kXWarp = 0;
 constexpr int kProducerWarp = 2;
 constexpr int kMmaWarp = 3;          // MMA issuer of M-tile 0 (and TMEM owner)
@@ -326,18 +296,21 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.kv_empty[s], MT + (EXTRA ? 1 : 0));   // one per MMA issuer (+ extra warp)
+      mbar_init(&sm.kv_empty[s], MT + (EXTRA ? kXWarps : 0));   // MMA issuers, extra warps
     }
     for (int m = 0; m < MT; ++m) {
-      mbar_init(&sm.s_full[m], 1);
-      mbar_init(&sm.p_full[m], 128);
+      mbar_init(&sm.s_full[m][0], 1);
+      mbar_init(&sm.s_full[m][1], 1);
+      mbar_init(&sm.p_full[m], 4);                    // one per softmax warp of the M-tile
       mbar_init(&sm.o_done[m], 1);
+      mbar_init(&sm.mma_done[m], 1);
     }
-    for (int m = 0; m < MT; ++m) mbar_init(&sm.mma_done[m], 1);
+    mbar_init(&sm.x_done, kXWarps);
     sm.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   {
+    // stale ring rows are multiplied by P = 0; zero keeps them finite
     uint4* kv = reinterpret_cast<uint4*>(&sm.k[0][0]);
     const int n16 = 2 * kStages * kBN * 128 / 16;     // k and v rings are contiguous
     for (int i = threadIdx.x; i < n16; i += blockDim.x) kv[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -351,6 +324,12 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     }
     fence_proxy_async();
   }
+  // Visible-table entries for the producer, 32 at a time (one per lane): the
+  // entry lookups are dependent global loads, so a batch costs one latency.
+  const int e_first = (int)((long long)t0 * kBN / Ps);
+  int e_batch = e_first & ~31, e_page = 0, e_len = 0;
+  if (warp == kProducerWarp && e_batch + lane < a.n_entries)
+    table_entry(a.tbl, e_batch + lane, e_page, e_len);
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
                      smem_u32(&sm.tmem_base)),
@@ -365,34 +344,50 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
 
   if (warp == kProducerWarp) {
     // ================================================================ producer
-    if (lane == 0) {
-      int issued_tiles = 0;
-      const int per = Ps >= kBN ? 1 : kBN / Ps;
-      const int rows = Ps >= kBN ? kBN : Ps;
-      for (int j = 0; j < nT; ++j) {
-        const int s = j % kStages;
-        if (!mbar_wait(&sm.kv_empty[s], ((j / kStages) & 1) ^ 1, abort, a.err)) break;
-        const int tile = t0 + j;
-        uint64_t mlo, mhi;
-        tile_mask(a, tile, mlo, mhi);
-        sm.mask[s][0] = mlo;
-        sm.mask[s][1] = mhi;
-        uint32_t bytes = 0;
-        for (int pp = 0; pp < per; ++pp)
-          if ((tile * kBN + pp * rows) / Ps < a.n_entries) bytes += 2u * rows * 128u;
-        mbar_arrive_expect_tx(&sm.kv_full[s], bytes);
-        for (int pp = 0; pp < per; ++pp) {
-          const int f0 = tile * kBN + pp * rows;
-          const int e = f0 / Ps, so = f0 - e * Ps;
-          if (e >= a.n_entries) break;
-          int page, len;
-          table_entry(a.tbl, e, page, len);
+    // The whole warp walks the tiles (its lanes hold the cached table entries);
+    // lane 0 issues the copies.
+    int issued_tiles = 0;
+    const int per = Ps >= kBN ? 1 : kBN / Ps;      // page blocks per tile
+    const int rows = Ps >= kBN ? kBN : Ps;         // slots per block
+    for (int j = 0; j < nT; ++j) {
+      const int s = j % kStages;
+      if (!mbar_wait(&sm.kv_empty[s], ((j / kStages) & 1) ^ 1, abort, a.err)) break;
+      const int tile = t0 + j;
+      uint64_t bits = 0;
+      int nblk = 0, blk_page[kBN / 16], blk_so[kBN / 16];
+#pragma unroll
+      for (int pp = 0; pp < kBN / 16; ++pp) {
+        if (pp >= per) break;
+        const int f0 = tile * kBN + pp * rows;
+        const int e = f0 / Ps, so = f0 - e * Ps;
+        if (e >= a.n_entries) break;
+        if ((e & ~31) != e_batch) {                // warp-uniform: next batch of entries
+          e_batch = e & ~31;
+          e_page = e_len = 0;
+          if (e_batch + lane < a.n_entries) table_entry(a.tbl, e_batch + lane, e_page, e_len);
+        }
+        const int page = __shfl_sync(0xffffffffu, e_page, e - e_batch);
+        const int len = __shfl_sync(0xffffffffu, e_len, e - e_batch);
+        int n = len - so;
+        n = n < 0 ? 0 : (n > rows ? rows : n);
+        if (n > 0) bits |= (n == 64 ? ~0ull : ((1ull << n) - 1ull)) << (pp * rows);
+        blk_page[pp] = page;
+        blk_so[pp] = so;
+        nblk = pp + 1;
+      }
+      if (lane == 0) {
+        sm.mask[s] = bits;
+        mbar_arrive_expect_tx(&sm.kv_full[s], (uint32_t)nblk * 2u * rows * 128u);
+#pragma unroll
+        for (int pp = 0; pp < kBN / 16; ++pp) {
+          if (pp >= nblk) break;
+          int page = blk_page[pp];
           if (page < 0 || page >= a.pool_pages) {
             atomicOr(a.err, kErrPageRange);
             page = 0;
           }
           const uint16_t* kp = a.pool + (long long)page * a.page_elems +
-                               ((long long)h * Ps + so) * kHeadDim;
+                               ((long long)h * Ps + blk_so[pp]) * kHeadDim;
           const uint16_t* vp = kp + (long long)H * Ps * kHeadDim;
           const uint32_t dk = smem_u32(&sm.k[s][pp * rows * 128]);
           const uint32_t dv = smem_u32(&sm.v[s][pp * rows * 128]);
@@ -408,51 +403,51 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
               "l"(vp), "r"((uint32_t)rows * 128u), "r"(mb)
               : "memory");
         }
-        issued_tiles = j + 1;
       }
-      // make sure no copy is still landing in shared memory when the CTA ends
+      issued_tiles = j + 1;
+    }
+    // make sure no copy is still landing in shared memory when the CTA ends
+    if (lane == 0)
       for (int j = issued_tiles - 1; j >= 0 && j >= issued_tiles - kStages; --j)
         mbar_wait(&sm.kv_full[j % kStages], (j / kStages) & 1, abort, a.err, false);
-    }
   } else if (warp == kMmaWarp || (MT == 2 && warp == kMmaWarp2)) {
     // ============================================================ MMA issuers
-    // One issuing thread per M-tile (warp 3: M-tile 0; warp 1: M-tile 1). An
-    // issuing thread stalls on each tcgen05.mma until the tensor core accepts
-    // it, so a single issuer for both M-tiles would make each M-tile's next QK
-    // wait behind the other's PV. Per M-tile, in order:
-    //   QK(m, j)    tile j in shared memory, and P_m of tile j-1 written (the
-    //               softmax has read S_m);
-    //   PV(m, j-1)  right after: it finishes while the softmax works on tile j,
-    //               which needs it done only before overwriting P_m;
+    // One issuing thread per M-tile (warp 3: M-tile 0; warp 1: M-tile 1): an
+    // issuing thread stalls on each tcgen05.mma until the tensor core takes it,
+    // and two issuers keep the tensor core twice as busy. Per M-tile, in order:
+    //   QK(m, j)    as soon as tile j is in shared memory, into S buffer j & 1
+    //               (its previous tile, j - 2, was exponentiated and its PV
+    //               issued earlier in this thread's order);
+    //   PV(m, j-1)  once the softmax has written P_m of tile j - 1;
     //   then one arrival on the stage of tile j-1 when those MMAs complete.
+    // The MMAs of one thread run in issue order, so QK(m, j+1) overwrites a
+    // buffer only after PV(m, j-1) has read the P stored in it.
     if (lane == 0) {
       const int m = warp == kMmaWarp ? 0 : 1;
       constexpr uint32_t kIdQK = idesc_bf16(128, kBN, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, kHeadDim, true);
       const uint64_t qa = sdesc(smem_u32(&sm.q[m][0]));
+      const uint32_t t_o = tmem + TmemCols<MT>::kO + m * kHeadDim;
       for (int j = 0; j <= nT && nT > 0; ++j) {
         if (j < nT) {
           if (!mbar_wait(&sm.kv_full[j % kStages], (j / kStages) & 1, abort, a.err)) break;
-        }
-        if (j > 0) {
-          if (!mbar_wait(&sm.p_full[m], (j - 1) & 1, abort, a.err)) break;
-        }
-        tc_fence_after();
-        if (j < nT) {
+          tc_fence_after();
           const uint64_t kb = sdesc(smem_u32(&sm.k[j % kStages][0]));
+          const uint32_t t_s = tmem + kBN * (2 * m + (j & 1));
 #pragma unroll
           for (int kk = 0; kk < kHeadDim / 16; ++kk)
-            tc_mma(tmem + m * kBN, qa + 2 * kk, kb + 2 * kk, kIdQK, kk > 0);
-          tc_commit(&sm.s_full[m]);
+            tc_mma(t_s, qa + 2 * kk, kb + 2 * kk, kIdQK, kk > 0);
+          tc_commit(&sm.s_full[m][j & 1]);
         }
         if (j > 0) {
           const int jp = j - 1;
+          if (!mbar_wait(&sm.p_full[m], jp & 1, abort, a.err)) break;
+          tc_fence_after();
           const uint64_t vb = sdesc(smem_u32(&sm.v[jp % kStages][0]));
+          const uint32_t t_p = tmem + kBN * (2 * m + (jp & 1));
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            tc_mma_ts(tmem + TmemCols<MT>::kO + m * kHeadDim,
-                      tmem + TmemCols<MT>::kP + m * (kBN / 2) + 8 * kk, vb + 128 * kk, kIdPV,
-                      (jp > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_ts(t_o, t_p + 8 * kk, vb + 128 * kk, kIdPV, (jp > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&sm.o_done[m]);
           tc_commit(&sm.kv_empty[jp % kStages]);
         }
@@ -461,7 +456,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
       tc_commit(&sm.mma_done[m]);
       mbar_wait(&sm.mma_done[m], 0, abort, a.err, false);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 4 + 4 * MT) {
     // ================================================================ softmax
     const int m = (warp - 4) >> 2;
     const int wq = warp & 3;                       // TMEM lane quarter of this warp
@@ -469,123 +464,87 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     const int row = row0 + m * 128 + r;
     const bool warp_active = row0 + m * 128 + wq * 32 < a.n_q;
     const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
-    const uint32_t t_s = tmem + t_lane + m * kBN;
     const uint32_t t_o = tmem + t_lane + TmemCols<MT>::kO + m * kHeadDim;
-    const uint32_t t_p = tmem + t_lane + TmemCols<MT>::kP + m * (kBN / 2);
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;          // running max (log2 units) and sum
     bool alive = true;
+    // o_done phases this warp has seen complete. A parity wait on phase n is
+    // exact only while the barrier has completed n or n + 1 phases, so the warp
+    // confirms PV(j-1) at the end of every tile j: PV(j) cannot have started
+    // then (it waits for this warp), and PV(j-1), issued when tile j began, has
+    // normally finished during the exponentials.
+    int o_seen = 0;
+    auto wait_pv = [&](int upto) -> bool {       // PV of tiles 0 .. upto completed
+      for (; o_seen <= upto; ++o_seen)
+        if (!mbar_wait(&sm.o_done[m], o_seen & 1, abort, a.err)) return false;
+      tc_fence_after();
+      return true;
+    };
     for (int j = 0; j < nT; ++j) {
       const int st = j % kStages;
-      if (!mbar_wait(&sm.s_full[m], j & 1, abort, a.err)) {
+      const uint32_t t_s = tmem + t_lane + kBN * (2 * m + (j & 1));
+      if (!mbar_wait(&sm.s_full[m][j & 1], (j >> 1) & 1, abort, a.err)) {
         alive = false;
         break;
       }
       tc_fence_after();
-      // the stage's slot mask (its tile cannot be replaced before this P is used)
+      // the stage's slot mask (the stage is not refilled before PV of this tile)
       if (!mbar_wait(&sm.kv_full[st], (j / kStages) & 1, abort, a.err)) {
         alive = false;
         break;
       }
-      const uint64_t mlo = sm.mask[st][0], mhi = sm.mask[st][1];
-      const bool full = (mlo & mhi) == ~0ull;
-      // Fast path: exponentiate against the running max of the earlier tiles and
-      // track this tile's max on the way, 64 columns at a time. Any reference
-      // keeps the result exact (it cancels in O / l); it only has to keep
-      // 2^(s - m) finite, so the exact path (tile max first, O rescaled) runs on
-      // the first tile and when the max has grown by more than 2^64.
-      uint32_t pk[kBN / 2];                        // P row as bf16 pairs
+      const uint64_t bits = sm.mask[st];
       bool rescale = false;
       float alpha = 1.f;
-      float sum0 = 0.f, sum1 = 0.f;
-      bool redo = m_run == -INFINITY;
-      if (warp_active && !redo) {
-        const float m_ref = m_run;
-        float t0m = -INFINITY, t1m = -INFINITY;
+      if (warp_active) {
+        float v[kBN];
+        PKV_TMEM_LD32(t_s, reinterpret_cast<uint32_t*>(v));
+        PKV_TMEM_LD32(t_s + 32, reinterpret_cast<uint32_t*>(v + 32));
+        tmem_wait_ld();
+        if (bits != ~0ull) {
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float v[64];
-          PKV_TMEM_LD32(t_s + 64 * hf, reinterpret_cast<uint32_t*>(&v[0]));
-          PKV_TMEM_LD32(t_s + 64 * hf + 32, reinterpret_cast<uint32_t*>(&v[32]));
-          tmem_wait_ld();
-          const uint64_t bits = hf ? mhi : mlo;
-          if (!full) {
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (!((bits >> c) & 1ull)) v[c] = -INFINITY;
-          }
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            t0m = fmaxf(t0m, v[c]);
-            t1m = fmaxf(t1m, v[c + 1]);
-            const float p0 = fast_exp2(fmaf(v[c], sl2, -m_ref));
-            const float p1 = fast_exp2(fmaf(v[c + 1], sl2, -m_ref));
-            pk[32 * hf + (c >> 1)] = pack_bf16(p0, p1);
-            sum0 += p0;
-            sum1 += p1;
-          }
+          for (int c = 0; c < kBN; ++c)
+            if (!((bits >> c) & 1ull)) v[c] = -INFINITY;
         }
-        redo = fmaxf(t0m, t1m) * sl2 > m_ref + kOverflowGuard;
-      }
-      if (__any_sync(0xffffffffu, warp_active && redo)) {
-        // exact path for the whole warp: S again from TMEM (QK(m, j+1) waits for P)
-        if (warp_active) {
-          float mx = -INFINITY;
+        // The reference max only has to keep 2^(s - m) finite (any reference
+        // cancels in O / l): it moves to the row max on the first tile and when
+        // the max has grown by more than 2^64, and O and l are rescaled then.
+        float x0 = -INFINITY, x1 = -INFINITY, x2 = -INFINITY, x3 = -INFINITY;
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            float v[64];
-            PKV_TMEM_LD32(t_s + 64 * hf, reinterpret_cast<uint32_t*>(&v[0]));
-            PKV_TMEM_LD32(t_s + 64 * hf + 32, reinterpret_cast<uint32_t*>(&v[32]));
-            tmem_wait_ld();
-            const uint64_t bits = hf ? mhi : mlo;
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if ((bits >> c) & 1ull) mx = fmaxf(mx, v[c]);
-          }
-          mx *= sl2;                               // sl2 > 0: max commutes with the scale
-          const float m_new = fmaxf(m_run, mx);
-          if (m_run != -INFINITY && m_new > m_run) {
-            alpha = fast_exp2(m_run - m_new);
+        for (int c = 0; c < kBN; c += 4) {
+          x0 = fmaxf(x0, v[c]);
+          x1 = fmaxf(x1, v[c + 1]);
+          x2 = fmaxf(x2, v[c + 2]);
+          x3 = fmaxf(x3, v[c + 3]);
+        }
+        const float tmax = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)) * sl2;   // sl2 > 0
+        if (tmax > m_run + kOverflowGuard) {       // also true on the first tile with a valid slot
+          if (m_run != -INFINITY) {
+            alpha = fast_exp2(m_run - tmax);
             l_run *= alpha;
             rescale = true;
           }
-          m_run = m_new;
-          const float m_ref = m_run == -INFINITY ? 0.f : m_run;
-          sum0 = sum1 = 0.f;
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            float v[64];
-            PKV_TMEM_LD32(t_s + 64 * hf, reinterpret_cast<uint32_t*>(&v[0]));
-            PKV_TMEM_LD32(t_s + 64 * hf + 32, reinterpret_cast<uint32_t*>(&v[32]));
-            tmem_wait_ld();
-            const uint64_t bits = hf ? mhi : mlo;
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (!((bits >> c) & 1ull)) v[c] = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-              const float p0 = fast_exp2(fmaf(v[c], sl2, -m_ref));
-              const float p1 = fast_exp2(fmaf(v[c + 1], sl2, -m_ref));
-              pk[32 * hf + (c >> 1)] = pack_bf16(p0, p1);
-              sum0 += p0;
-              sum1 += p1;
-            }
-          }
+          m_run = tmax;
         }
-      }
-      if (!warp_active) {
+        const float m_ref = m_run == -INFINITY ? 0.f : m_run;
+        // P over the S buffer it came from (bf16 pairs in its first 32 columns)
+        uint32_t pk[kBN / 2];
+        float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-        for (int c = 0; c < kBN / 2; ++c) pk[c] = 0u;
-      }
-      l_run += sum0 + sum1;
-      // PV of the previous tile must be done before P_m is overwritten and
-      // before O_m is rescaled
-      if (j > 0) {
-        if (!mbar_wait(&sm.o_done[m], (j - 1) & 1, abort, a.err)) {
-          alive = false;
-          break;
+        for (int c = 0; c < kBN; c += 2) {
+          const float p0 = fast_exp2(fmaf(v[c], sl2, -m_ref));
+          const float p1 = fast_exp2(fmaf(v[c + 1], sl2, -m_ref));
+          pk[c >> 1] = pack_bf16(p0, p1);
+          sum0 += p0;
+          sum1 += p1;
         }
-        tc_fence_after();
+        l_run += sum0 + sum1;
+        PKV_TMEM_ST32(t_s, pk);
+        tmem_wait_st();
+      }
+      if (!wait_pv(j - 1)) {
+        alive = false;
+        break;
       }
       if (__any_sync(0xffffffffu, rescale)) {
         // O_m *= alpha for this row (alpha = 1 for rows that keep their max)
@@ -600,22 +559,13 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
         }
         tmem_wait_st();
       }
-      // P row (bf16 pairs) into TMEM, where PV reads its A operand
-      if (warp_active) {
-        PKV_TMEM_ST32(t_p, pk);
-        PKV_TMEM_ST32(t_p + 32, (&pk[32]));
-        tmem_wait_st();
-      }
-      // S_m has been read and P_m written: QK(m, j+1) and PV(m, j) may go
+      // S_m read, P_m written, O_m rescaled: PV(m, j) may go
       tc_fence_before();
-      mbar_arrive(&sm.p_full[m]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_full[m]);
     }
     // ---- epilogue: O_m row to the output (or the split's partial), 16 columns at a time
-    bool have_o = false;
-    if (alive && nT > 0) {
-      have_o = mbar_wait(&sm.o_done[m], (nT - 1) & 1, abort, a.err);
-      if (have_o) tc_fence_after();
-    }
+    const bool have_o = alive && nT > 0 && wait_pv(nT - 1);
     const bool write = alive && row < a.n_q && (have_o || nT == 0);
     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
     const long long ro = ((long long)split * a.n_q + row) * H + h;
@@ -646,13 +596,16 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     }
     if (write && a.num_splits > 1)
       *reinterpret_cast<float2*>(a.part_ml + ro * 2) = make_float2(m_run, l_run);
-  } else if (EXTRA && warp == kXWarp) {
+  } else if (EXTRA && (warp == kXWarp || warp >= 4 + 4 * MT)) {
     // ============================================== extra rows (mma.sync, regs)
-    // Up to 8 query rows, transposed so that the 8 queries are the N = 8 side of
-    // m16n8k16 tiles and the slots the M = 16 side: S^T = K Q_x^T (8 tiles of
-    // 16 slots per 128-slot tile), then O^T += V^T P^T with P^T moved into B
-    // fragments by movmatrix. Softmax runs over slots, i.e. across the 8 lanes
-    // that share a query column.
+    // Up to 8 query rows, shared by kXWarps warps: warp xi takes slots 16 xi ..
+    // 16 xi + 15 of every tile with its own running max, sum and O, and the
+    // partial results are merged at the end. Transposed so that the 8 queries
+    // are the N = 8 side of m16n8k16 tiles and the slots the M = 16 side:
+    // S^T = K Q_x^T, then O^T += V^T P^T with P^T moved into B fragments by
+    // movmatrix. Softmax runs over slots, i.e. across the 8 lanes that share a
+    // query column.
+    const int xi = warp == kXWarp ? 0 : warp - (4 + 4 * MT) + 1;
     const int xr0 = row0 + MT * 128;               // first extra row
     const int g = lane >> 2, tq = lane & 3;
     // B fragments of Q_x^T: (k = d 2tq.., n = query g)
@@ -681,32 +634,25 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
         alive = false;
         break;
       }
-      const uint64_t mlo = sm.mask[st][0], mhi = sm.mask[st][1];
+      const uint64_t bits = sm.mask[st];
       const uint32_t kbase = smem_u32(&sm.k[st][0]), vbase = smem_u32(&sm.v[st][0]);
-      // S^T (128 slots x 8 queries) in 8 slot-tiles of 16
-      float sc[8][4];
+      // S^T: this warp's 16 slots x 8 queries
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          uint32_t ka[4];
-          ldsm_x4(sw_addr(kbase, mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * kk + (lane >> 4)),
-                  ka[0], ka[1], ka[2], ka[3]);
-          mma_16816(sc[mt], ka, qb[kk][0], qb[kk][1]);
-        }
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t ka[4];
+        ldsm_x4(sw_addr(kbase, xi * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * kk + (lane >> 4)),
+                ka[0], ka[1], ka[2], ka[3]);
+        mma_16816(sc, ka, qb[kk][0], qb[kk][1]);
       }
-      // mask, scale, per-query max over the tile's slots
+      // mask, scale, per-query max over the warp's slots
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int slot = mt * 16 + g + (e >> 1) * 8;
-          const bool ok = ((slot < 64 ? mlo : mhi) >> (slot & 63)) & 1ull;
-          sc[mt][e] = ok ? sc[mt][e] * sl2 : -INFINITY;
-          mx[e & 1] = fmaxf(mx[e & 1], sc[mt][e]);
-        }
+      for (int e = 0; e < 4; ++e) {
+        const bool ok = (bits >> (xi * 16 + g + (e >> 1) * 8)) & 1ull;
+        sc[e] = ok ? sc[e] * sl2 : -INFINITY;
+        mx[e & 1] = fmaxf(mx[e & 1], sc[e]);
+      }
       float alpha[2], m_use[2];
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
@@ -726,26 +672,23 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
         ox[dt][2] *= alpha[0];
         ox[dt][3] *= alpha[1];
       }
-      // P^T, then O^T += V^T P^T per 16-slot k-step
+      // P^T, then O^T += V^T P^T over the warp's 16 slots
+      const float p0 = fast_exp2(sc[0] - m_use[0]);
+      const float p1 = fast_exp2(sc[1] - m_use[1]);
+      const float p2 = fast_exp2(sc[2] - m_use[0]);
+      const float p3 = fast_exp2(sc[3] - m_use[1]);
+      l_x[0] += p0 + p2;
+      l_x[1] += p1 + p3;
+      // (slot g | g+8, query 2tq..) pairs -> transposed: (query g, slots 2tq..)
+      uint32_t pb0 = pack_bf16(p0, p1), pb1 = pack_bf16(p2, p3);
+      asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %0;\n" : "+r"(pb0));
+      asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %0;\n" : "+r"(pb1));
 #pragma unroll
-      for (int kp = 0; kp < 8; ++kp) {
-        const float p0 = fast_exp2(sc[kp][0] - m_use[0]);
-        const float p1 = fast_exp2(sc[kp][1] - m_use[1]);
-        const float p2 = fast_exp2(sc[kp][2] - m_use[0]);
-        const float p3 = fast_exp2(sc[kp][3] - m_use[1]);
-        l_x[0] += p0 + p2;
-        l_x[1] += p1 + p3;
-        // (slot g | g+8, query 2tq..) pairs -> transposed: (query g, slots 2tq..)
-        uint32_t pb0 = pack_bf16(p0, p1), pb1 = pack_bf16(p2, p3);
-        asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %0;\n" : "+r"(pb0));
-        asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %0;\n" : "+r"(pb1));
-#pragma unroll
-        for (int dt = 0; dt < 4; ++dt) {
-          uint32_t va[4];
-          ldsm_x4_t(sw_addr(vbase, kp * 16 + (lane & 7) + (lane >> 4) * 8, 2 * dt + ((lane >> 3) & 1)),
-                    va[0], va[1], va[2], va[3]);
-          mma_16816(ox[dt], va, pb0, pb1);
-        }
+      for (int dt = 0; dt < 4; ++dt) {
+        uint32_t va[4];
+        ldsm_x4_t(sw_addr(vbase, xi * 16 + (lane & 7) + (lane >> 4) * 8, 2 * dt + ((lane >> 3) & 1)),
+                  va[0], va[1], va[2], va[3]);
+        mma_16816(ox[dt], va, pb0, pb1);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.kv_empty[st]);
@@ -756,26 +699,54 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
       l_x[qq] += __shfl_xor_sync(0xffffffffu, l_x[qq], 8);
       l_x[qq] += __shfl_xor_sync(0xffffffffu, l_x[qq], 16);
     }
+    // publish this warp's partial state; warp 0 merges the kXWarps of them
 #pragma unroll
     for (int qq = 0; qq < 2; ++qq) {
-      const int xrow = xr0 + 2 * tq + qq;
-      if (!alive || xrow >= a.n_q) continue;
-      const float inv = l_x[qq] > 0.f ? 1.f / l_x[qq] : 0.f;
-      const long long ro = ((long long)split * a.n_q + xrow) * H + h;
 #pragma unroll
       for (int dt = 0; dt < 4; ++dt)
 #pragma unroll
-        for (int hi = 0; hi < 2; ++hi) {
-          const int d = dt * 16 + g + hi * 8;
-          const float val = ox[dt][2 * hi + qq];
-          if (a.num_splits == 1)
-            a.out[((long long)xrow * H + h) * kHeadDim + d] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(val * inv));
-          else
-            a.part_o[ro * kHeadDim + d] = val;
+        for (int hi = 0; hi < 2; ++hi) sm.xo[xi][2 * tq + qq][dt * 16 + g + hi * 8] = ox[dt][2 * hi + qq];
+      if (g == 0) {
+        sm.xml[xi][2 * tq + qq][0] = m_x[qq];
+        sm.xml[xi][2 * tq + qq][1] = l_x[qq];
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.x_done);
+    if (xi == 0 && alive && mbar_wait(&sm.x_done, 0, abort, a.err)) {
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        const int xq = 2 * tq + qq;
+        const int xrow = xr0 + xq;
+        if (xrow >= a.n_q) continue;
+        float mm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kXWarps; ++i) mm = fmaxf(mm, sm.xml[i][xq][0]);
+        float w[kXWarps], ll = 0.f;
+#pragma unroll
+        for (int i = 0; i < kXWarps; ++i) {
+          w[i] = mm == -INFINITY ? 0.f : fast_exp2(sm.xml[i][xq][0] - mm);
+          ll += w[i] * sm.xml[i][xq][1];
         }
-      if (a.num_splits > 1 && g == 0)
-        *reinterpret_cast<float2*>(a.part_ml + ro * 2) = make_float2(m_x[qq], l_x[qq]);
+        const float inv = ll > 0.f ? 1.f / ll : 0.f;
+        const long long ro = ((long long)split * a.n_q + xrow) * H + h;
+#pragma unroll
+        for (int dt = 0; dt < 4; ++dt)
+#pragma unroll
+          for (int hi = 0; hi < 2; ++hi) {
+            const int d = dt * 16 + g + hi * 8;
+            float val = 0.f;
+#pragma unroll
+            for (int i = 0; i < kXWarps; ++i) val += w[i] * sm.xo[i][xq][d];
+            if (a.num_splits == 1)
+              a.out[((long long)xrow * H + h) * kHeadDim + d] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(val * inv));
+            else
+              a.part_o[ro * kHeadDim + d] = val;
+          }
+        if (a.num_splits > 1 && g == 0)
+          *reinterpret_cast<float2*>(a.part_ml + ro * 2) = make_float2(mm, ll);
+      }
     }
   }
 

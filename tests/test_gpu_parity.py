@@ -84,12 +84,12 @@ def test_tiny_golden_trace_on_gpu():
         pr.evict(sid)
 
 
-@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("seed", range(8))
 def test_random_frame_streams(seed):
     """Random small configurations with keyframes, rollbacks and windowed resets;
     two layers so that layer > 0 appends and per-layer resets are covered."""
     rng = random.Random(seed)
-    ps = rng.choice([16, 32, 64, 128])
+    ps = rng.choice([16, 32, 64, 128, 192])
     S = rng.randint(1, 3)
     windowed = seed % 2 == 1
     w = WORKLOADS["tiny"].with_(page_size=ps, n_patch=ps, n_special=rng.randint(1, 6), num_scale=S,
