@@ -44,16 +44,19 @@ constexpr int kBN = 64;            // slots per KV tile
 constexpr int kStages = 8;         // KV ring depth
 constexpr int kXRows = 8;          // extra query rows handled with mma.sync
 constexpr int kXWarps = kBN / 16;  // extra-row warps: one 16-slot quarter of a tile each
-// TMEM columns (fp32): S_m buffer b at 64 (2m + b) (P_m of that tile overwrites
-// its first 32 columns as bf16 pairs), O_m at 128 MT + 64m; the allocation is a
-// power of two.
+// TMEM columns: S_m buffer b (fp32) at 64 (2m + b), O_m (fp32) at 128 MT + 64m,
+// P_m buffer b (bf16 pairs, 32 columns for 64 slots) at 192 MT + 32 (2m + b);
+// 512 columns for two M-tiles, 256 for one.
 template <int MT>
 struct TmemCols {
   static constexpr int kO = 128 * MT;
+  static constexpr int kP = 192 * MT;
   static constexpr int kAlloc = MT == 1 ? 256 : 512;
 };
 constexpr uint32_t kSpinLimit = 1u << 25;
-constexpr float kOverflowGuard = 64.0f;     // log2 units: p stays below 2^64
+// A tile is exponentiated against the running reference max; if a row's sum of
+// 2^(s - m) exceeds 2^64 (or overflows), the row's reference moves to its max.
+constexpr float kSumLimit = 18446744073709551616.0f;   // 2^64
 
 template <int MT>
 struct __align__(1024) TcSmem {
@@ -66,7 +69,7 @@ struct __align__(1024) TcSmem {
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[MT][2];            // S_m of the buffer's latest tile is in TMEM
-  uint64_t p_full[MT];               // P_m of the latest tile is in TMEM (O_m rescaled)
+  uint64_t p_full[MT];               // P_m of the latest tile is in TMEM, S_m read, O_m rescaled
   uint64_t o_done[MT];               // PV of the latest tile has completed
   uint64_t mma_done[MT];
   uint64_t x_done;                   // the extra-row warps have published their partials
@@ -414,43 +417,43 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     // ============================================================ MMA issuers
     // One issuing thread per M-tile (warp 3: M-tile 0; warp 1: M-tile 1): an
     // issuing thread stalls on each tcgen05.mma until the tensor core takes it,
-    // and two issuers keep the tensor core twice as busy. Per M-tile, in order:
-    //   QK(m, j)    as soon as tile j is in shared memory, into S buffer j & 1
-    //               (its previous tile, j - 2, was exponentiated and its PV
-    //               issued earlier in this thread's order);
-    //   PV(m, j-1)  once the softmax has written P_m of tile j - 1;
-    //   then one arrival on the stage of tile j-1 when those MMAs complete.
-    // The MMAs of one thread run in issue order, so QK(m, j+1) overwrites a
-    // buffer only after PV(m, j-1) has read the P stored in it.
+    // and two issuers keep the tensor core twice as busy. S and P each have two
+    // TMEM buffers per M-tile, tile j using buffer j & 1. Per M-tile:
+    //   QK(m, 0), QK(m, 1) up front; then for every tile j, once the softmax
+    //   has read S and written P of tile j:
+    //   PV(m, j)      O_m += P_m V, then one arrival on the stage of tile j;
+    //   QK(m, j + 2)  into the S buffer tile j has just released, so S of the
+    //                 next tile is ready long before the softmax reaches it.
     if (lane == 0) {
       const int m = warp == kMmaWarp ? 0 : 1;
       constexpr uint32_t kIdQK = idesc_bf16(128, kBN, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, kHeadDim, true);
       const uint64_t qa = sdesc(smem_u32(&sm.q[m][0]));
       const uint32_t t_o = tmem + TmemCols<MT>::kO + m * kHeadDim;
-      for (int j = 0; j <= nT && nT > 0; ++j) {
-        if (j < nT) {
-          if (!mbar_wait(&sm.kv_full[j % kStages], (j / kStages) & 1, abort, a.err)) break;
-          tc_fence_after();
-          const uint64_t kb = sdesc(smem_u32(&sm.k[j % kStages][0]));
-          const uint32_t t_s = tmem + kBN * (2 * m + (j & 1));
+      auto issue_qk = [&](int j) -> bool {
+        if (!mbar_wait(&sm.kv_full[j % kStages], (j / kStages) & 1, abort, a.err)) return false;
+        tc_fence_after();
+        const uint64_t kb = sdesc(smem_u32(&sm.k[j % kStages][0]));
+        const uint32_t t_s = tmem + kBN * (2 * m + (j & 1));
 #pragma unroll
-          for (int kk = 0; kk < kHeadDim / 16; ++kk)
-            tc_mma(t_s, qa + 2 * kk, kb + 2 * kk, kIdQK, kk > 0);
-          tc_commit(&sm.s_full[m][j & 1]);
-        }
-        if (j > 0) {
-          const int jp = j - 1;
-          if (!mbar_wait(&sm.p_full[m], jp & 1, abort, a.err)) break;
-          tc_fence_after();
-          const uint64_t vb = sdesc(smem_u32(&sm.v[jp % kStages][0]));
-          const uint32_t t_p = tmem + kBN * (2 * m + (jp & 1));
+        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+          tc_mma(t_s, qa + 2 * kk, kb + 2 * kk, kIdQK, kk > 0);
+        tc_commit(&sm.s_full[m][j & 1]);
+        return true;
+      };
+      bool ok = nT < 1 || issue_qk(0);
+      ok = ok && (nT < 2 || issue_qk(1));
+      for (int j = 0; ok && j < nT; ++j) {
+        if (!mbar_wait(&sm.p_full[m], j & 1, abort, a.err)) break;
+        tc_fence_after();
+        const uint64_t vb = sdesc(smem_u32(&sm.v[j % kStages][0]));
+        const uint32_t t_p = tmem + TmemCols<MT>::kP + (kBN / 2) * (2 * m + (j & 1));
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            tc_mma_ts(t_o, t_p + 8 * kk, vb + 128 * kk, kIdPV, (jp > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&sm.o_done[m]);
-          tc_commit(&sm.kv_empty[jp % kStages]);
-        }
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          tc_mma_ts(t_o, t_p + 8 * kk, vb + 128 * kk, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&sm.o_done[m]);
+        tc_commit(&sm.kv_empty[j % kStages]);
+        if (j + 2 < nT && !issue_qk(j + 2)) break;
       }
       // every MMA issued by this thread has completed once mma_done[m] flips
       tc_commit(&sm.mma_done[m]);
@@ -472,7 +475,8 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     // exact only while the barrier has completed n or n + 1 phases, so the warp
     // confirms PV(j-1) at the end of every tile j: PV(j) cannot have started
     // then (it waits for this warp), and PV(j-1), issued when tile j began, has
-    // normally finished during the exponentials.
+    // normally finished during the exponentials. It also frees the P buffer
+    // that tile j + 1 writes.
     int o_seen = 0;
     auto wait_pv = [&](int upto) -> bool {       // PV of tiles 0 .. upto completed
       for (; o_seen <= upto; ++o_seen)
@@ -494,9 +498,16 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
         break;
       }
       const uint64_t bits = sm.mask[st];
+      const uint32_t t_p = tmem + t_lane + TmemCols<MT>::kP + (kBN / 2) * (2 * m + (j & 1));
       bool rescale = false;
       float alpha = 1.f;
       if (warp_active) {
+        // Fast path: exponentiate against the running reference max. Any
+        // reference keeps the result exact (it cancels in O / l); it only has
+        // to keep 2^(s - m) finite, so a row whose sum exceeds 2^64 (or is not
+        // finite), and every row on its first tile, takes the exact path: its
+        // reference moves to its max and O and l are rescaled. S stays in TMEM
+        // until this tile's arrival below, so the exact path reads it again.
         float v[kBN];
         PKV_TMEM_LD32(t_s, reinterpret_cast<uint32_t*>(v));
         PKV_TMEM_LD32(t_s + 32, reinterpret_cast<uint32_t*>(v + 32));
@@ -506,40 +517,62 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
           for (int c = 0; c < kBN; ++c)
             if (!((bits >> c) & 1ull)) v[c] = -INFINITY;
         }
-        // The reference max only has to keep 2^(s - m) finite (any reference
-        // cancels in O / l): it moves to the row max on the first tile and when
-        // the max has grown by more than 2^64, and O and l are rescaled then.
-        float x0 = -INFINITY, x1 = -INFINITY, x2 = -INFINITY, x3 = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kBN; c += 4) {
-          x0 = fmaxf(x0, v[c]);
-          x1 = fmaxf(x1, v[c + 1]);
-          x2 = fmaxf(x2, v[c + 2]);
-          x3 = fmaxf(x3, v[c + 3]);
-        }
-        const float tmax = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)) * sl2;   // sl2 > 0
-        if (tmax > m_run + kOverflowGuard) {       // also true on the first tile with a valid slot
-          if (m_run != -INFINITY) {
-            alpha = fast_exp2(m_run - tmax);
-            l_run *= alpha;
-            rescale = true;
-          }
-          m_run = tmax;
-        }
-        const float m_ref = m_run == -INFINITY ? 0.f : m_run;
-        // P over the S buffer it came from (bf16 pairs in its first 32 columns)
         uint32_t pk[kBN / 2];
         float sum0 = 0.f, sum1 = 0.f;
+        {
+          const float m_ref = m_run == -INFINITY ? 0.f : m_run;
 #pragma unroll
-        for (int c = 0; c < kBN; c += 2) {
-          const float p0 = fast_exp2(fmaf(v[c], sl2, -m_ref));
-          const float p1 = fast_exp2(fmaf(v[c + 1], sl2, -m_ref));
-          pk[c >> 1] = pack_bf16(p0, p1);
-          sum0 += p0;
-          sum1 += p1;
+          for (int c = 0; c < kBN; c += 2) {
+            const float p0 = fast_exp2(fmaf(v[c], sl2, -m_ref));
+            const float p1 = fast_exp2(fmaf(v[c + 1], sl2, -m_ref));
+            pk[c >> 1] = pack_bf16(p0, p1);
+            sum0 += p0;
+            sum1 += p1;
+          }
+        }
+        const bool redo = m_run == -INFINITY || !(sum0 + sum1 <= kSumLimit);
+        if (__any_sync(0xffffffffu, redo)) {
+          // exact path for the rows that need it (the TMEM load is warp-wide)
+          PKV_TMEM_LD32(t_s, reinterpret_cast<uint32_t*>(v));
+          PKV_TMEM_LD32(t_s + 32, reinterpret_cast<uint32_t*>(v + 32));
+          tmem_wait_ld();
+          if (redo) {
+            float x0 = -INFINITY, x1 = -INFINITY, x2 = -INFINITY, x3 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kBN; c += 4) {
+              if (!((bits >> c) & 1ull)) v[c] = -INFINITY;
+              if (!((bits >> (c + 1)) & 1ull)) v[c + 1] = -INFINITY;
+              if (!((bits >> (c + 2)) & 1ull)) v[c + 2] = -INFINITY;
+              if (!((bits >> (c + 3)) & 1ull)) v[c + 3] = -INFINITY;
+              x0 = fmaxf(x0, v[c]);
+              x1 = fmaxf(x1, v[c + 1]);
+              x2 = fmaxf(x2, v[c + 2]);
+              x3 = fmaxf(x3, v[c + 3]);
+            }
+            const float tmax = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)) * sl2;   // sl2 > 0
+            if (tmax > m_run) {                    // -inf stays -inf: no valid slot yet
+              if (m_run != -INFINITY) {
+                alpha = fast_exp2(m_run - tmax);
+                l_run *= alpha;
+                rescale = true;
+              }
+              m_run = tmax;
+            }
+            const float m_ref = m_run == -INFINITY ? 0.f : m_run;
+            sum0 = sum1 = 0.f;
+#pragma unroll
+            for (int c = 0; c < kBN; c += 2) {
+              const float p0 = fast_exp2(fmaf(v[c], sl2, -m_ref));
+              const float p1 = fast_exp2(fmaf(v[c + 1], sl2, -m_ref));
+              pk[c >> 1] = pack_bf16(p0, p1);
+              sum0 += p0;
+              sum1 += p1;
+            }
+          }
         }
         l_run += sum0 + sum1;
-        PKV_TMEM_ST32(t_s, pk);
+        // P into its buffer (PV of tile j - 2, which read it, has completed)
+        PKV_TMEM_ST32(t_p, pk);
         tmem_wait_st();
       }
       if (!wait_pv(j - 1)) {
@@ -559,7 +592,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
         }
         tmem_wait_st();
       }
-      // S_m read, P_m written, O_m rescaled: PV(m, j) may go
+      // S_m read, P_m written, O_m rescaled: PV(m, j) and QK(m, j + 2) may go
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.p_full[m]);
