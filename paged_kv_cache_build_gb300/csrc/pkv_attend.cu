@@ -32,39 +32,45 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // Merge the splits' partial (o, m, l) of each (row, head): 16 threads per pair,
 // four head_dim elements each; every thread reads all the splits' (m, l) (the 16
 // threads of a pair share them through L1) and its four elements of each o.
-constexpr int kMaxSplits = 16;
 
-__global__ void __launch_bounds__(256) combine_kernel(const AttendArgs a) {
+__global__ void __launch_bounds__(256, 2) combine_kernel(const AttendArgs a) {
   const long long n_pairs = (long long)a.n_q * a.heads;
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long pair = gid >> 4;
   const int q4 = (int)(gid & 15);
   if (pair >= n_pairs) return;
   const int S = a.num_splits;
-  float m[kMaxSplits], l[kMaxSplits];
-  float m_max = -INFINITY;
-#pragma unroll
-  for (int s = 0; s < kMaxSplits; ++s) {
-    if (s < S) {
-      const float2 ml = __ldg(reinterpret_cast<const float2*>(a.part_ml + (s * n_pairs + pair) * 2));
-      m[s] = ml.x;
-      l[s] = ml.y;
-      if (ml.y > 0.f) m_max = fmaxf(m_max, ml.x);
-    }
-  }
-  float l_sum = 0.f;
+  // Eight splits at a time: their loads are issued together, then folded into
+  // the running max, sum and O. Every split writes its partials (an empty one
+  // as max -inf, sum 0, O 0).
+  float m_run = -INFINITY, l_sum = 0.f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < S; s0 += 8) {
+    float2 ml[8];
+    float4 ov[8];
 #pragma unroll
-  for (int s = 0; s < kMaxSplits; ++s) {
-    if (s < S && l[s] > 0.f) {
-      const float w = fast_exp2(m[s] - m_max);
-      const float4 ov =
-          __ldg(reinterpret_cast<const float4*>(a.part_o + (s * n_pairs + pair) * kHeadDim) + q4);
-      l_sum += w * l[s];
-      o.x += w * ov.x;
-      o.y += w * ov.y;
-      o.z += w * ov.z;
-      o.w += w * ov.w;
+    for (int i = 0; i < 8; ++i) {
+      ml[i] = make_float2(-INFINITY, 0.f);
+      ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s0 + i < S) {
+        const long long sp = (long long)(s0 + i) * n_pairs + pair;
+        ml[i] = __ldg(reinterpret_cast<const float2*>(a.part_ml + sp * 2));
+        ov[i] = __ldg(reinterpret_cast<const float4*>(a.part_o + sp * kHeadDim) + q4);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (ml[i].y > 0.f) {
+        const float m_new = fmaxf(m_run, ml[i].x);
+        const float c = fast_exp2(m_run - m_new);     // 0 while m_run is -inf
+        const float w = fast_exp2(ml[i].x - m_new);
+        l_sum = l_sum * c + w * ml[i].y;
+        o.x = o.x * c + w * ov[i].x;
+        o.y = o.y * c + w * ov[i].y;
+        o.z = o.z * c + w * ov[i].z;
+        o.w = o.w * c + w * ov[i].w;
+        m_run = m_new;
+      }
     }
   }
   const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
