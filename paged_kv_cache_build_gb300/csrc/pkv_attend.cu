@@ -34,6 +34,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // threads of a pair share them through L1) and its four elements of each o.
 
 __global__ void __launch_bounds__(256, 2) combine_kernel(const AttendArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const long long n_pairs = (long long)a.n_q * a.heads;
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long pair = gid >> 4;
@@ -89,9 +91,9 @@ cudaError_t launch_attend(const AttendArgs& a, int num_sms, cudaStream_t s) {
   cudaError_t e = launch_attend_tc(a, s);
   if (e != cudaSuccess || a.num_splits == 1) return e;
   const long long threads = (long long)a.n_q * a.heads * 16;
-  combine_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(a);
+  e = launch_pdl(combine_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, s, a);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace pkv

@@ -317,6 +317,18 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     uint4* kv = reinterpret_cast<uint4*>(&sm.k[0][0]);
     const int n16 = 2 * kStages * kBN * 128 / 16;     // k and v rings are contiguous
     for (int i = threadIdx.x; i < n16; i += blockDim.x) kv[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                     smem_u32(&sm.tmem_base)),
+                 "r"(TmemCols<MT>::kAlloc));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+  // everything above is private to the CTA; inputs are read only after the
+  // previous kernel on the stream has completed
+  pdl_wait();
+  pdl_trigger();
+  {
     for (int i = threadIdx.x; i < MT * 128 * 8; i += blockDim.x) {
       const int m = i / (128 * 8), r = (i >> 3) & 127, c = i & 7;
       const int row = row0 + m * 128 + r;
@@ -333,12 +345,6 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   int e_batch = e_first & ~31, e_page = 0, e_len = 0;
   if (warp == kProducerWarp && e_batch + lane < a.n_entries)
     table_entry(a.tbl, e_batch + lane, e_page, e_len);
-  if (warp == kMmaWarp) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
-                     smem_u32(&sm.tmem_base)),
-                 "r"(TmemCols<MT>::kAlloc));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -804,9 +810,10 @@ cudaError_t launch_mt(const AttendArgs& a, int n_mgroups, int n_tiles, cudaStrea
     configured = true;
   }
   const int grid = n_mgroups * a.heads * a.num_splits;
-  attend_tc_kernel<MT, EXTRA><<<grid, tc_threads<MT, EXTRA>(), smem, s>>>(a, n_mgroups, n_tiles);
+  const cudaError_t e = launch_pdl(attend_tc_kernel<MT, EXTRA>, dim3(grid), dim3(tc_threads<MT, EXTRA>()),
+                                   smem, s, a, n_mgroups, n_tiles);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 struct TcShape {

@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <utility>
 #include <stdint.h>
 
 namespace pkv {
@@ -201,6 +203,36 @@ struct AttendArgs {
 };
 
 // Kernel launches made by this library in this process (every launcher counts).
+// ---------------------------------------------------- dependent launches
+// The frame path's kernels are launched with programmatic stream serialization:
+// a kernel may start while the one before it on the stream finishes, does only
+// CTA-private set-up (shared memory, TMEM, mbarriers) until pdl_wait(), and
+// every thread of every CTA executes pdl_wait() before it touches global memory
+// or exits. pdl_wait() returns once the previous kernel has completed and its
+// writes are visible; since that kernel waited for its own predecessor before
+// completing, the order of the whole stream is kept. pdl_trigger() lets the
+// next kernel start launching early. Both are no-ops for a normal launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 unsigned long long launch_count();
 void count_launches(int n);
 

@@ -36,6 +36,8 @@ __device__ __forceinline__ uint16_t* row_ptr(const PoolView& pv, int page, int k
 // the batch's page needs (1, or 2 when the frame opens a special page), so stream
 // i pops after streams 0..i-1 exactly as sequential appends would.
 __global__ void __launch_bounds__(512) frame_append_kernel(const FrameAppendArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.y;
   __shared__ int s_patch, s_sp;
   if (threadIdx.x < 32) {
@@ -103,6 +105,8 @@ __global__ void __launch_bounds__(512) frame_append_kernel(const FrameAppendArgs
 // per token, as above; the first blocks also zero the tail of a freshly popped
 // last page.
 __global__ void __launch_bounds__(512) chunk_append_kernel(const ChunkAppendArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int Ps = a.pool.page_size;
   if (a.is_meta && blockIdx.x == 0) {
     for (int i = threadIdx.x; i < a.n_new; i += blockDim.x) {
@@ -149,6 +153,8 @@ __global__ void __launch_bounds__(512) chunk_append_kernel(const ChunkAppendArgs
 // Push page ids onto the free stack: free[top + j] for j over the segments in
 // order. Sources are stream lists, never the free stack itself.
 __global__ void __launch_bounds__(256) push_kernel(const PushArgs a) {
+  pdl_wait();
+  pdl_trigger();
   int total = 0;
   for (int s = 0; s < a.n_seg; ++s) total += a.seg[s].count;
   for (int j = threadIdx.x; j < total; j += blockDim.x) {
@@ -294,21 +300,23 @@ void count_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
 
 cudaError_t launch_frame_append(const FrameAppendArgs& a, cudaStream_t s) {
   dim3 grid(a.n_patch + a.n_special, a.n);
-  frame_append_kernel<<<grid, 16 * a.pool.heads < 32 ? 32 : 16 * a.pool.heads, 0, s>>>(a);
+  const cudaError_t e =
+      launch_pdl(frame_append_kernel, grid, dim3(16 * a.pool.heads < 32 ? 32 : 16 * a.pool.heads), 0, s, a);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_chunk_append(const ChunkAppendArgs& a, cudaStream_t s) {
-  chunk_append_kernel<<<a.n_tokens, 16 * a.pool.heads < 32 ? 32 : 16 * a.pool.heads, 0, s>>>(a);
+  const cudaError_t e = launch_pdl(chunk_append_kernel, dim3(a.n_tokens),
+                                   dim3(16 * a.pool.heads < 32 ? 32 : 16 * a.pool.heads), 0, s, a);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_push(const PushArgs& a, cudaStream_t s) {
-  push_kernel<<<1, 256, 0, s>>>(a);
+  const cudaError_t e = launch_pdl(push_kernel, dim3(1), dim3(256), 0, s, a);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_reset_copy(const ResetCopyArgs& a, cudaStream_t s) {
