@@ -17,21 +17,23 @@
 //                tensor-core operand; no tensor map is needed.
 //   warps 3, 1   MMA issuers (one thread each, one per M-tile): S_m = Q_m K^T
 //                (N = 64 slots) into one of two TMEM buffers, and O_m += P_m V
-//                with P_m read from TMEM.
-//   warps 4..    one warpgroup per M-tile (a thread per query row): reads its S
-//                row from TMEM, masks invalid slots, keeps a running max (only
-//                raised when it grows by more than 2^64), and writes P = 2^(S - m)
-//                as bf16 over the S buffer it came from, where PV takes its A
-//                operand; at the end it reads O from TMEM.
-//   warps 0, 4+4MT..  the extra rows (at most 8, if any), one 16-slot quarter of
+//                with P_m read from one of two TMEM buffers.
+//   warps 4..11  one warpgroup per M-tile (a thread per query row): reads its S
+//                row from TMEM, masks invalid slots, exponentiates against the
+//                row's running reference max (moved to the row max on the first
+//                tile and when the row's sum would exceed 2^64), writes P =
+//                2^(S - m) as bf16 into TMEM, where PV takes its A operand, and at
+//                the end reads O from TMEM.
+//   warps 0, 12-14  the extra rows (at most 8, if any), one 16-slot quarter of
 //                every tile per warp, through warp-level mma.sync tiles held in
 //                registers; an M = 128 tensor-core tile for 6 rows would cost as
 //                much as a full one.
-// With two S buffers per M-tile, QK of tile j+1 runs while the softmax works on
-// tile j, and PV of tile j while the softmax works on tile j+1; the softmax
-// (its exponentials) sets the pace. Every mbarrier wait is bounded; a wait that
-// gives up sets the device error word, and the CTA drains its copies and MMAs
-// and frees TMEM before returning.
+// With two S and two P buffers per M-tile, QK of tile j+2 is issued as soon as
+// the softmax releases tile j, and PV of tile j runs while the softmax works on
+// tile j+1; the softmax (its exponentials) and the tensor-core queue set the
+// pace. Every mbarrier wait is bounded; a wait that gives up sets the device
+// error word, and the CTA drains its copies and MMAs and frees TMEM before
+// returning.
 #include <cuda_bf16.h>
 
 #include "pkv_internal.cuh"
