@@ -605,33 +605,32 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.p_full[m]);
     }
-    // ---- epilogue: O_m row to the output (or the split's partial), 16 columns at a time
+    // ---- epilogue: O_m row (64 columns, one TMEM read) to the output or the split's partial
     const bool have_o = alive && nT > 0 && wait_pv(nT - 1);
     const bool write = alive && row < a.n_q && (have_o || nT == 0);
     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
     const long long ro = ((long long)split * a.n_q + row) * H + h;
+    uint32_t o[kHeadDim];
 #pragma unroll
-    for (int c = 0; c < kHeadDim; c += 16) {
-      uint32_t o[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) o[i] = 0u;
-      if (have_o && warp_active) {
-        PKV_TMEM_LD16(t_o + c, o);
-        tmem_wait_ld();
-      }
-      if (!write) continue;
+    for (int i = 0; i < kHeadDim; ++i) o[i] = 0u;
+    if (have_o && warp_active) {
+      PKV_TMEM_LD32(t_o, o);
+      PKV_TMEM_LD32(t_o + 32, (o + 32));
+      tmem_wait_ld();
+    }
+    if (write) {
       if (a.num_splits == 1) {
-        uint4* dst = reinterpret_cast<uint4*>(a.out + ((long long)row * H + h) * kHeadDim + c);
+        uint4* dst = reinterpret_cast<uint4*>(a.out + ((long long)row * H + h) * kHeadDim);
 #pragma unroll
-        for (int q4 = 0; q4 < 2; ++q4) {
+        for (int q4 = 0; q4 < 8; ++q4) {
           const float* f = reinterpret_cast<const float*>(&o[8 * q4]);
           dst[q4] = make_uint4(pack_bf16(f[0] * inv, f[1] * inv), pack_bf16(f[2] * inv, f[3] * inv),
                                pack_bf16(f[4] * inv, f[5] * inv), pack_bf16(f[6] * inv, f[7] * inv));
         }
       } else {
-        uint4* dst = reinterpret_cast<uint4*>(a.part_o + ro * kHeadDim + c);
+        uint4* dst = reinterpret_cast<uint4*>(a.part_o + ro * kHeadDim);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
+        for (int q4 = 0; q4 < 16; ++q4)
           dst[q4] = make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
       }
     }
