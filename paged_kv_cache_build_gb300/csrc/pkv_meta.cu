@@ -30,11 +30,22 @@ __device__ __forceinline__ uint16_t* row_ptr(const PoolView& pv, int page, int k
          ((long long)(kv * pv.heads + head) * pv.page_size + slot) * kHeadDim;
 }
 
-// One batched frame-mode append. blockIdx.y selects the stream, blockIdx.x the
-// token; thread (kv, head, 16-byte chunk) moves one vector. Every block
+// Tokens moved by one append block (TPB): with several, each thread issues all
+// its loads before its stores and the block's set-up (page-need scan, barrier)
+// is shared; a single frame keeps one token per block so that it still spreads
+// over the SMs.
+template <int TPB>
+constexpr int append_blocks(int tokens) { return (tokens + TPB - 1) / TPB; }
+constexpr int kAppendBatchTokens = 8;
+constexpr long long kAppendBatchMin = 4096;   // tokens x streams above which TPB = 8
+
+// One batched frame-mode append. blockIdx.y selects the stream, blockIdx.x a
+// group of TPB tokens; thread (kv, head, 16-byte chunk) moves one vector per
+// token. Every block
 // recomputes its stream's place on the free stack with an exclusive warp scan of
 // the batch's page needs (1, or 2 when the frame opens a special page), so stream
 // i pops after streams 0..i-1 exactly as sequential appends would.
+template <int TPB>
 __global__ void __launch_bounds__(512) frame_append_kernel(const FrameAppendArgs a) {
   pdl_wait();
   pdl_trigger();
@@ -82,28 +93,39 @@ __global__ void __launch_bounds__(512) frame_append_kernel(const FrameAppendArgs
   if (hh >= 2 * H) return;                   // blocks have at least one full warp
   const int kv = hh >= H ? 1 : 0;
   const int h = hh - kv * H;
-  const int t = blockIdx.x;
-  // token t of the frame
-  {
-    const uint16_t* src = (kv ? it.v : it.k) + ((long long)t * H + h) * kHeadDim + c * 8;
-    const uint4 val = __ldg(reinterpret_cast<const uint4*>(src));
-    const int page = t < a.n_patch ? patch : sp;
-    const int slot = t < a.n_patch ? t : it.sp_off + (t - a.n_patch);
-    *reinterpret_cast<uint4*>(row_ptr(a.pool, page, kv, h, slot) + swizzle_chunk(slot, c) * 8) = val;
-  }
-  // a freshly opened special page gets its unused slots zeroed, so that every
-  // slot of a held page is a token or zero
-  if (it.new_sp && t < a.pool.page_size - a.n_special) {
-    const int slot = a.n_special + t;
-    *reinterpret_cast<uint4*>(row_ptr(a.pool, sp, kv, h, slot) + swizzle_chunk(slot, c) * 8) =
-        make_uint4(0u, 0u, 0u, 0u);
+  const int T = a.n_patch + a.n_special;
+  const int t0 = blockIdx.x * TPB;
+  const uint16_t* src = (kv ? it.v : it.k) + (long long)h * kHeadDim + c * 8;
+  uint4 val[TPB];
+#pragma unroll
+  for (int i = 0; i < TPB; ++i)
+    if (t0 + i < T)
+      val[i] = __ldg(reinterpret_cast<const uint4*>(src + (long long)(t0 + i) * H * kHeadDim));
+#pragma unroll
+  for (int i = 0; i < TPB; ++i) {
+    const int t = t0 + i;
+    if (t < T) {
+      const int page = t < a.n_patch ? patch : sp;
+      const int slot = t < a.n_patch ? t : it.sp_off + (t - a.n_patch);
+      *reinterpret_cast<uint4*>(row_ptr(a.pool, page, kv, h, slot) + swizzle_chunk(slot, c) * 8) =
+          val[i];
+    }
+    // a freshly opened special page gets its unused slots zeroed, so that every
+    // slot of a held page is a token or zero (the grid covers page_size +
+    // n_special > page_size - n_special token indices)
+    if (it.new_sp && t < a.pool.page_size - a.n_special) {
+      const int slot = a.n_special + t;
+      *reinterpret_cast<uint4*>(row_ptr(a.pool, sp, kv, h, slot) + swizzle_chunk(slot, c) * 8) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
   }
 }
 
 // Chunked-mode append: the frame's tokens are packed after the chunk's pos0
 // tokens; pages of the chunk past old_pages are popped by this append. One block
-// per token, as above; the first blocks also zero the tail of a freshly popped
+// per TPB tokens, as above; the blocks also zero the tail of a freshly popped
 // last page.
+template <int TPB>
 __global__ void __launch_bounds__(512) chunk_append_kernel(const ChunkAppendArgs a) {
   pdl_wait();
   pdl_trigger();
@@ -123,20 +145,8 @@ __global__ void __launch_bounds__(512) chunk_append_kernel(const ChunkAppendArgs
   if (hh >= 2 * H) return;
   const int kv = hh >= H ? 1 : 0;
   const int h = hh - kv * H;
-  const int t = blockIdx.x;
-  // pass 0: token t; passes 1..: tail slots t, t + gridDim.x, ...
-  for (int pass = 0;; ++pass) {
-    int pos;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (pass == 0) {
-      pos = a.pos0 + t;
-      const uint16_t* src = (kv ? a.v : a.k) + ((long long)t * H + h) * kHeadDim + c * 8;
-      val = __ldg(reinterpret_cast<const uint4*>(src));
-    } else {
-      const int z = t + (pass - 1) * (int)gridDim.x;
-      if (z >= zero_slots) break;
-      pos = end + z;
-    }
+  // position pos of the chunk receives val (a token, or zero past the end)
+  auto put = [&](int pos, const uint4& val) {
     const int pi = pos / Ps;
     const int slot = pos - pi * Ps;
     const int page = (pi < a.old_pages || !a.is_meta)
@@ -144,10 +154,25 @@ __global__ void __launch_bounds__(512) chunk_append_kernel(const ChunkAppendArgs
                          : a.free_stack[a.top - 1 - (pi - a.old_pages)];
     if (!page_ok(page, a.pool.pool_pages)) {
       atomicOr(a.err, kErrPageRange);
-      continue;
+      return;
     }
     *reinterpret_cast<uint4*>(row_ptr(a.pool, page, kv, h, slot) + swizzle_chunk(slot, c) * 8) = val;
-  }
+  };
+  // tokens t0 .. t0 + TPB - 1, loads first
+  const int t0 = blockIdx.x * TPB;
+  const uint16_t* src = (kv ? a.v : a.k) + (long long)h * kHeadDim + c * 8;
+  uint4 val[TPB];
+#pragma unroll
+  for (int i = 0; i < TPB; ++i)
+    if (t0 + i < a.n_tokens)
+      val[i] = __ldg(reinterpret_cast<const uint4*>(src + (long long)(t0 + i) * H * kHeadDim));
+#pragma unroll
+  for (int i = 0; i < TPB; ++i)
+    if (t0 + i < a.n_tokens) put(a.pos0 + t0 + i, val[i]);
+  // the unused tail of a freshly popped last page, in groups of TPB slots
+  for (int z0 = t0; z0 < zero_slots; z0 += (int)gridDim.x * TPB)
+    for (int i = 0; i < TPB && z0 + i < zero_slots; ++i)
+      put(end + z0 + i, make_uint4(0u, 0u, 0u, 0u));
 }
 
 // Push page ids onto the free stack: free[top + j] for j over the segments in
@@ -299,16 +324,24 @@ unsigned long long launch_count() { return g_launches.load(); }
 void count_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
 
 cudaError_t launch_frame_append(const FrameAppendArgs& a, cudaStream_t s) {
-  dim3 grid(a.n_patch + a.n_special, a.n);
+  const int T = a.n_patch + a.n_special;
+  const dim3 block(16 * a.pool.heads < 32 ? 32 : 16 * a.pool.heads);
   const cudaError_t e =
-      launch_pdl(frame_append_kernel, grid, dim3(16 * a.pool.heads < 32 ? 32 : 16 * a.pool.heads), 0, s, a);
+      (long long)T * a.n >= kAppendBatchMin
+          ? launch_pdl(frame_append_kernel<kAppendBatchTokens>,
+                       dim3(append_blocks<kAppendBatchTokens>(T), a.n), block, 0, s, a)
+          : launch_pdl(frame_append_kernel<1>, dim3(T, a.n), block, 0, s, a);
   count_launches(1);
   return e;
 }
 
 cudaError_t launch_chunk_append(const ChunkAppendArgs& a, cudaStream_t s) {
-  const cudaError_t e = launch_pdl(chunk_append_kernel, dim3(a.n_tokens),
-                                   dim3(16 * a.pool.heads < 32 ? 32 : 16 * a.pool.heads), 0, s, a);
+  const dim3 block(16 * a.pool.heads < 32 ? 32 : 16 * a.pool.heads);
+  const cudaError_t e =
+      a.n_tokens >= kAppendBatchMin
+          ? launch_pdl(chunk_append_kernel<kAppendBatchTokens>,
+                       dim3(append_blocks<kAppendBatchTokens>(a.n_tokens)), block, 0, s, a)
+          : launch_pdl(chunk_append_kernel<1>, dim3(a.n_tokens), block, 0, s, a);
   count_launches(1);
   return e;
 }
