@@ -396,6 +396,74 @@ def extra_append(reps=20):
             "peak_source": kind}
 
 
+def extra_multistream(frames=100, reps=20):
+    """32 LingBot-shaped streams at steady state (`frames` frames each): one
+    frame's attention for every stream, as one pkv_attend_batched call and as 32
+    pkv_attend calls. frame-steps/s counts a stream's frame as one step."""
+    import ctypes
+    import torch
+    from paged_kv_cache_build_gb300 import PagedKVCache, frame_stream_cfg, synth_fill
+    from paged_kv_cache_build_gb300._lib import check
+    from synth import TENSOR_K, TENSOR_Q, TENSOR_V, WORKLOADS
+    w = WORKLOADS["multistream"]
+    n, T, H, D = w.streams, w.frame_tokens, w.heads, w.head_dim
+    cache = PagedKVCache(3072, w.page_size, H, D, max_streams=64)
+    sids = [cache.open_stream(frame_stream_cfg(w.num_scale, w.window, w.n_patch, w.n_special))
+            for _ in range(n)]
+    R = 8
+    kv = torch.empty((2, R, T, H, D), dtype=torch.bfloat16, device="cuda")
+    synth_fill(kv[0], 0, w.index, 0, 0, 0, TENSOR_K)
+    synth_fill(kv[1], 0, w.index, 0, 0, 0, TENSOR_V)
+    for t in range(frames):
+        for s in sids:
+            cache.append_frame(s, kv[0, t % R], kv[1, t % R])
+        if t < frames - 1:
+            for s in sids:
+                cache.evict_window(s)
+    q = torch.empty((n * T, H, D), dtype=torch.bfloat16, device="cuda")
+    synth_fill(q, 0, w.index, 0, 0, 0, TENSOR_Q, 0, w.q_scale)
+    out = torch.empty_like(q)
+    lib, h = cache.lib, cache.h
+    c_off = (ctypes.c_int * (n + 1))(*[i * T for i in range(n + 1)])
+    c_sids = (ctypes.c_int * n)(*sids)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    row = T * H * D * 2
+
+    def batched():
+        check(lib.pkv_attend_batched(h, ctypes.c_void_p(q.data_ptr()), c_off, c_sids, n, 0,
+                                     ctypes.c_void_p(out.data_ptr()), ctypes.c_float(w.sm_scale),
+                                     stream), h)
+
+    def separate():
+        for i, s in enumerate(sids):
+            check(lib.pkv_attend(h, ctypes.c_void_p(q.data_ptr() + i * row), T, s, 0,
+                                 ctypes.c_void_p(out.data_ptr() + i * row), ctypes.c_float(w.sm_scale),
+                                 stream), h)
+
+    res = {}
+    for name, fn in (("batched", batched), ("separate", separate)):
+        times = []
+        for r in range(reps + 3):
+            e0, e1 = _events()
+            torch.cuda._sleep(HOST_COVER_CYCLES)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 3:
+                times.append(e0.elapsed_time(e1))
+        res[name] = statistics.median(times)
+    n_kv = cache.visible_count(sids[0])[1]
+    flops = 4.0 * T * n_kv * D * H * n
+    cache.sync()
+    cache.close()
+    return {"workload": "32 LingBot-shaped streams x 262 queries, %d visible tokens each" % n_kv,
+            "ms_batched": round(res["batched"], 4), "ms_separate": round(res["separate"], 4),
+            "frame_steps_per_s_batched": round(n / (res["batched"] * 1e-3), 1),
+            "frame_steps_per_s_separate": round(n / (res["separate"] * 1e-3), 1),
+            "attn_tflops_batched": round(flops / (res["batched"] * 1e-3) / 1e12, 2)}
+
+
 # ------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -580,7 +648,8 @@ def run_ours(args):
         "clocks": clocks.summary(),
     }
     if not args.no_extra:
-        line["extra"] = {"chunked": extra_chunked(), "long24": extra_long24(), "append": extra_append()}
+        line["extra"] = {"chunked": extra_chunked(), "long24": extra_long24(), "append": extra_append(),
+                         "multistream": extra_multistream()}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)

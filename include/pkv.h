@@ -191,6 +191,22 @@ pkv_status pkv_attend(pkv_t h, const void* q, int n_q, int stream_id, int layer,
 pkv_status pkv_attend_chunked(pkv_t h, const void* q, int n_q, int stream_id, int layer,
                               void* out, float sm_scale, void* cuda_stream);
 
+/* Several streams' attention in one launch (the multi-stream pool of LingBot-Map
+ * section 4; batching in the manner of the vLLM-Omni RFC's scheduler, section
+ * 2.3). Equivalent to n calls of pkv_attend (frame-mode streams) or
+ * pkv_attend_chunked (chunked-mode streams) on the same cuda_stream, each over
+ * its own visible pages, with the same numerics; the split of the KV range into
+ * parallel parts is chosen for the whole batch, so results may differ from the
+ * separate calls by rounding.
+ * q, out: device bf16 [q_off[n]][heads][64], the streams' query rows back to
+ * back: rows q_off[i] .. q_off[i + 1] - 1 belong to stream sids[i].
+ * q_off (n + 1 ints, q_off[0] = 0, increasing) and sids (n distinct open
+ * streams) are host arrays; 1 <= n <= 32; every stream uses `layer`.
+ * Errors: INVALID for bad arguments, STATE if a stream has nothing visible (or,
+ * chunked, no open chunk); checked for every stream before anything is launched. */
+pkv_status pkv_attend_batched(pkv_t h, const void* q, const int* q_off, const int* sids, int n,
+                              int layer, void* out, float sm_scale, void* cuda_stream);
+
 /* Attention that allocates nothing (no counterpart in the paper; it serves callers
  * of this library).
  * Same inputs, outputs, numerics and errors as pkv_attend (frame-mode streams) and

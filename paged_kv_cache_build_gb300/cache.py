@@ -122,6 +122,25 @@ class PagedKVCache:
                                                 _stream_ptr(stream)))
         return out
 
+    def attend_batched(self, qs, sids, layer=0, sm_scale=0.0, stream=None):
+        """pkv_attend_batched: the streams' attention in one launch. qs: one
+        [n_q][heads][64] bf16 tensor per stream (packed into one buffer here);
+        returns one output tensor per stream."""
+        if len(qs) != len(sids):
+            raise ValueError("one query tensor per stream")
+        q = torch.cat([x.reshape(-1, self.heads, self.head_dim) for x in qs]).contiguous()
+        out = torch.empty_like(q)
+        off = [0]
+        for x in qs:
+            off.append(off[-1] + x.shape[0])
+        n = len(sids)
+        c_off = (ctypes.c_int * (n + 1))(*off)
+        c_sids = (ctypes.c_int * n)(*sids)
+        self._check(self.lib.pkv_attend_batched(self.h, _bf16_ptr(q, "q"), c_off, c_sids, n, layer,
+                                                _bf16_ptr(out, "out"), float(sm_scale),
+                                                _stream_ptr(stream)))
+        return [out[off[i]:off[i + 1]] for i in range(n)]
+
     def attend_noalloc(self, q, sid, layer=0, out=None, sm_scale=0.0, stream=None):
         """pkv_attend_noalloc: attention whose scratch is a fixed device array."""
         if out is None:

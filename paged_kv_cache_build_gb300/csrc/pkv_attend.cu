@@ -33,14 +33,28 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // four head_dim elements each; every thread reads all the splits' (m, l) (the 16
 // threads of a pair share them through L1) and its four elements of each o.
 
-__global__ void __launch_bounds__(256, 2) combine_kernel(const AttendArgs a) {
+// The call a thread's (query row, head) pair belongs to, and the pair's index in it.
+__device__ __forceinline__ const AttendArgs& pair_call(const AttendArgs& a, long long& pair) {
+  return a;
+}
+__device__ __forceinline__ const AttendArgs& pair_call(const AttendBatch& b, long long& pair) {
+  int i = 0;
+  while (i + 1 < b.n && pair >= b.pair_base[i + 1]) ++i;
+  pair -= b.pair_base[i];
+  return b.item[i];
+}
+
+template <typename Params>
+__global__ void __launch_bounds__(256, 2) combine_kernel(const __grid_constant__ Params params,
+                                                         long long total_pairs) {
   pdl_wait();
   pdl_trigger();
-  const long long n_pairs = (long long)a.n_q * a.heads;
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long pair = gid >> 4;
+  long long pair = gid >> 4;
   const int q4 = (int)(gid & 15);
-  if (pair >= n_pairs) return;
+  if (pair >= total_pairs) return;
+  const AttendArgs& a = pair_call(params, pair);
+  const long long n_pairs = (long long)a.n_q * a.heads;
   const int S = a.num_splits;
   // Eight splits at a time: their loads are issued together, then folded into
   // the running max, sum and O. Every split writes its partials (an empty one
@@ -90,8 +104,19 @@ cudaError_t launch_attend(const AttendArgs& a, int num_sms, cudaStream_t s) {
   (void)num_sms;
   cudaError_t e = launch_attend_tc(a, s);
   if (e != cudaSuccess || a.num_splits == 1) return e;
-  const long long threads = (long long)a.n_q * a.heads * 16;
-  e = launch_pdl(combine_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, s, a);
+  const long long pairs = (long long)a.n_q * a.heads;
+  e = launch_pdl(combine_kernel<AttendArgs>, dim3((unsigned)((pairs * 16 + 255) / 256)), dim3(256),
+                 0, s, a, pairs);
+  count_launches(1);
+  return e;
+}
+
+cudaError_t launch_attend_batch(const AttendBatch& b, cudaStream_t s) {
+  cudaError_t e = launch_attend_tc_batch(b, s);
+  if (e != cudaSuccess || b.item[0].num_splits == 1) return e;
+  const long long pairs = b.pair_base[b.n];
+  e = launch_pdl(combine_kernel<AttendBatch>, dim3((unsigned)((pairs * 16 + 255) / 256)), dim3(256),
+                 0, s, b, pairs);
   count_launches(1);
   return e;
 }

@@ -278,16 +278,33 @@ constexpr int kProducerWarp = 2;
 constexpr int kMmaWarp = 3;          // MMA issuer of M-tile 0 (and TMEM owner)
 constexpr int kMmaWarp2 = 1;         // MMA issuer of M-tile 1
 
-template <int MT, bool EXTRA>
+// The call a CTA works on: the launch's only one, or its stream's in a batch.
+struct CtaWork {
+  const AttendArgs* a;
+  int bid, n_mgroups, n_tiles;
+};
+__device__ __forceinline__ CtaWork cta_work(const AttendArgs& a, int n_mgroups, int n_tiles) {
+  return {&a, (int)blockIdx.x, n_mgroups, n_tiles};
+}
+__device__ __forceinline__ CtaWork cta_work(const AttendBatch& b, int, int) {
+  int i = 0;
+  while (i + 1 < b.n && (int)blockIdx.x >= b.cta_base[i + 1]) ++i;
+  return {&b.item[i], (int)blockIdx.x - b.cta_base[i], b.n_mgroups[i], b.n_tiles[i]};
+}
+
+template <int MT, bool EXTRA, typename Params>
 __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
-    attend_tc_kernel(const AttendArgs a, int n_mgroups, int n_tiles) {
+    attend_tc_kernel(const __grid_constant__ Params params, int n_mgroups_1, int n_tiles_1) {
   extern __shared__ uint8_t smem_raw[];
   TcSmem<MT>& sm = *reinterpret_cast<TcSmem<MT>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const CtaWork cw = cta_work(params, n_mgroups_1, n_tiles_1);
+  const AttendArgs& a = *cw.a;
+  const int n_mgroups = cw.n_mgroups, n_tiles = cw.n_tiles;
   const int H = a.heads, Ps = a.page_size;
 
-  int bid = blockIdx.x;
+  int bid = cw.bid;
   const int mg = bid % n_mgroups;
   bid /= n_mgroups;
   const int h = bid % H;
@@ -800,19 +817,18 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   }
 }
 
-template <int MT, bool EXTRA>
-cudaError_t launch_mt(const AttendArgs& a, int n_mgroups, int n_tiles, cudaStream_t s) {
+template <int MT, bool EXTRA, typename Params>
+cudaError_t launch_mt(const Params& p, int grid, int n_mgroups, int n_tiles, cudaStream_t s) {
   const size_t smem = sizeof(TcSmem<MT>) + 1024;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<MT, EXTRA>,
+    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<MT, EXTRA, Params>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int grid = n_mgroups * a.heads * a.num_splits;
-  const cudaError_t e = launch_pdl(attend_tc_kernel<MT, EXTRA>, dim3(grid), dim3(tc_threads<MT, EXTRA>()),
-                                   smem, s, a, n_mgroups, n_tiles);
+  const cudaError_t e = launch_pdl(attend_tc_kernel<MT, EXTRA, Params>, dim3(grid),
+                                   dim3(tc_threads<MT, EXTRA>()), smem, s, p, n_mgroups, n_tiles);
   count_launches(1);
   return e;
 }
@@ -839,17 +855,26 @@ int attend_tc_tiles(long long n_slots) { return (int)((n_slots + kBN - 1) / kBN)
 
 // Split-KV factor: fill the SMs in as few, as even waves as possible.
 int attend_tc_splits(int n_q, int heads, int n_tiles, int num_sms) {
+  return attend_tc_splits_pairs(tc_shape(n_q).n_mgroups * heads, n_tiles, num_sms);
+}
+
+int attend_tc_shape(int n_q) {
   const TcShape sh = tc_shape(n_q);
-  const int base = sh.n_mgroups * heads;
+  return (sh.mt - 1) * 2 + (sh.extra ? 1 : 0);
+}
+
+int attend_tc_mgroups(int n_q) { return tc_shape(n_q).n_mgroups; }
+
+int attend_tc_splits_pairs(int pairs, int n_tiles, int num_sms) {
+  // a wave's time is proportional to the tiles each CTA handles
   int best = 1;
   double best_eff = 0.0;
   for (int s = 1; s <= 16; ++s) {
     if (s > 1 && n_tiles / s < 3) break;
-    const int ctas = base * s;
+    const int ctas = pairs * s;
     const int waves = (ctas + num_sms - 1) / num_sms;
-    // a wave's time is proportional to the tiles each CTA handles
     const double t = (double)waves * ((double)n_tiles / s);
-    const double eff = (double)base * n_tiles / (t * num_sms);
+    const double eff = (double)pairs * n_tiles / (t * num_sms);
     if (eff > best_eff * 1.03) {
       best_eff = eff;
       best = s;
@@ -858,15 +883,26 @@ int attend_tc_splits(int n_q, int heads, int n_tiles, int num_sms) {
   return best;
 }
 
+template <typename Params>
+static cudaError_t launch_shape(int shape, const Params& p, int grid, int n_mgroups, int n_tiles,
+                                cudaStream_t s) {
+  switch (shape) {
+    case 0: return launch_mt<1, false>(p, grid, n_mgroups, n_tiles, s);
+    case 1: return launch_mt<1, true>(p, grid, n_mgroups, n_tiles, s);
+    case 2: return launch_mt<2, false>(p, grid, n_mgroups, n_tiles, s);
+    default: return launch_mt<2, true>(p, grid, n_mgroups, n_tiles, s);
+  }
+}
+
 cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t s) {
   const TcShape sh = tc_shape(a.n_q);
   const int n_tiles = attend_tc_tiles(a.n_slots);
-  if (sh.mt == 1) {
-    return sh.extra ? launch_mt<1, true>(a, sh.n_mgroups, n_tiles, s)
-                    : launch_mt<1, false>(a, sh.n_mgroups, n_tiles, s);
-  }
-  return sh.extra ? launch_mt<2, true>(a, sh.n_mgroups, n_tiles, s)
-                  : launch_mt<2, false>(a, sh.n_mgroups, n_tiles, s);
+  return launch_shape(attend_tc_shape(a.n_q), a, sh.n_mgroups * a.heads * a.num_splits,
+                      sh.n_mgroups, n_tiles, s);
+}
+
+cudaError_t launch_attend_tc_batch(const AttendBatch& b, cudaStream_t s) {
+  return launch_shape(attend_tc_shape(b.item[0].n_q), b, b.cta_base[b.n], 0, 0, s);
 }
 
 }  // namespace pkv

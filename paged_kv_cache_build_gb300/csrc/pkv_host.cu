@@ -14,6 +14,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -739,8 +740,10 @@ static pkv_status ensure_scratch(pkv_t h, size_t bytes) {
   return PKV_OK;
 }
 
-static pkv_status attend_common(pkv_t h, Stream* st, const void* q, int n_q, int layer, void* out,
-                                float sm_scale, cudaStream_t s) {
+// The attention arguments of one call on one stream, split count and scratch
+// aside.
+static pkv_status attend_args(pkv_t h, Stream* st, const void* q, int n_q, int layer, void* out,
+                              float sm_scale, AttendArgs* a) {
   if (!q || !out || !aligned16(q) || !aligned16(out))
     return fail(h, PKV_ERR_INVALID, "q/out must be 16-byte aligned device pointers");
   if (n_q < 1 || n_q > (1 << 20)) return fail(h, PKV_ERR_INVALID, "n_q %d out of range", n_q);
@@ -748,32 +751,46 @@ static pkv_status attend_common(pkv_t h, Stream* st, const void* q, int n_q, int
   int np, nt, last;
   visible_counts(h, *st, &np, &nt, &last);
   if (nt == 0) return fail(h, PKV_ERR_STATE, "nothing is visible");
-  AttendArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.q = static_cast<const uint16_t*>(q);
-  a.out = static_cast<uint16_t*>(out);
-  a.n_q = n_q;
-  a.heads = h->H;
-  a.pool = h->d_pool + (long long)layer * h->P * h->page_elems;
-  a.page_elems = h->page_elems;
-  a.page_size = h->Ps;
-  a.pool_pages = h->P;
-  a.tbl_idx = st->d_tbl_idx;
-  a.tbl_len = st->d_tbl_len;
-  a.tbl = table_args(h, *st, st->d_tbl_idx, st->d_tbl_len, nullptr, nullptr);
-  a.n_entries = np;
-  a.n_slots = (long long)(np - 1) * h->Ps + last;
-  a.n_tiles = ceil_div(a.n_slots, 64);
+  std::memset(a, 0, sizeof(*a));
+  a->q = static_cast<const uint16_t*>(q);
+  a->out = static_cast<uint16_t*>(out);
+  a->n_q = n_q;
+  a->heads = h->H;
+  a->pool = h->d_pool + (long long)layer * h->P * h->page_elems;
+  a->page_elems = h->page_elems;
+  a->page_size = h->Ps;
+  a->pool_pages = h->P;
+  a->tbl_idx = st->d_tbl_idx;
+  a->tbl_len = st->d_tbl_len;
+  a->tbl = table_args(h, *st, st->d_tbl_idx, st->d_tbl_len, nullptr, nullptr);
+  a->n_entries = np;
+  a->n_slots = (long long)(np - 1) * h->Ps + last;
+  a->n_tiles = ceil_div(a->n_slots, 64);
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)h->D);
-  a.scale_log2 = scale * 1.4426950408889634f;
+  a->scale_log2 = scale * 1.4426950408889634f;
+  a->num_splits = 1;
+  a->err = h->d_err;
+  return PKV_OK;
+}
+
+static size_t partial_bytes(const AttendArgs& a) {
+  return (size_t)a.num_splits * a.n_q * a.heads * (kHeadDim + 2) * sizeof(float);
+}
+
+// Split-KV partials of `a` at `base`: O first, then the (max, sum) pairs.
+static void place_partials(AttendArgs* a, float* base) {
+  a->part_o = base;
+  a->part_ml = base + (size_t)a->num_splits * a->n_q * a->heads * kHeadDim;
+}
+
+static pkv_status attend_common(pkv_t h, Stream* st, const void* q, int n_q, int layer, void* out,
+                                float sm_scale, cudaStream_t s) {
+  AttendArgs a;
+  if (pkv_status r = attend_args(h, st, q, n_q, layer, out, sm_scale, &a)) return r;
   a.num_splits = attend_num_splits(n_q, h->H, a.n_slots, h->num_sms);
-  a.err = h->d_err;
   if (a.num_splits > 1) {
-    const size_t o_bytes = (size_t)a.num_splits * n_q * h->H * kHeadDim * sizeof(float);
-    const size_t ml_bytes = (size_t)a.num_splits * n_q * h->H * 2 * sizeof(float);
-    if (pkv_status r = ensure_scratch(h, o_bytes + ml_bytes)) return r;
-    a.part_o = h->d_scratch;
-    a.part_ml = h->d_scratch + o_bytes / sizeof(float);
+    if (pkv_status r = ensure_scratch(h, partial_bytes(a))) return r;
+    place_partials(&a, h->d_scratch);
   }
   PKV_CUDA(h, launch_attend(a, h->num_sms, s));
   return PKV_OK;
@@ -799,6 +816,80 @@ pkv_status pkv_attend_chunked(pkv_t h, const void* q, int n_q, int sid, int laye
   if (n_q != st->c_len[cur])
     return fail(h, PKV_ERR_INVALID, "n_q %d != the open chunk's %d tokens", n_q, st->c_len[cur]);
   return attend_common(h, st, q, n_q, layer, out, sm_scale, as_stream(cuda_stream));
+}
+
+pkv_status pkv_attend_batched(pkv_t h, const void* q, const int* q_off, const int* sids, int n,
+                              int layer, void* out, float sm_scale, void* cuda_stream) {
+  if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
+  if (n < 1 || n > kMaxBatch || !q_off || !sids || !q || !out)
+    return fail(h, PKV_ERR_INVALID, "need 1..%d streams, offsets, ids, q and out", kMaxBatch);
+  if (q_off[0] != 0) return fail(h, PKV_ERR_INVALID, "q_off[0] must be 0");
+  const size_t row_bytes = (size_t)h->H * kHeadDim * sizeof(uint16_t);
+  // every stream's call, validated before anything is launched
+  std::vector<AttendArgs> calls(n);
+  for (int i = 0; i < n; ++i) {
+    for (int k = 0; k < i; ++k)
+      if (sids[k] == sids[i]) return fail(h, PKV_ERR_INVALID, "stream %d listed twice", sids[i]);
+    Stream* st = nullptr;
+    if (pkv_status r = get_stream(h, sids[i], &st)) return r;
+    const int n_q = q_off[i + 1] - q_off[i];
+    if (n_q < 1 || q_off[i + 1] > (1 << 20))
+      return fail(h, PKV_ERR_INVALID, "stream %d: query rows %d..%d", sids[i], q_off[i], q_off[i + 1]);
+    if (st->cfg.mode == PKV_MODE_CHUNKED) {
+      if (!st->c_open) return fail(h, PKV_ERR_STATE, "stream %d: no open chunk", sids[i]);
+      const int cur = (st->c_head + st->n_chunks - 1) % st->cfg.sliding_window_num;
+      if (n_q != st->c_len[cur])
+        return fail(h, PKV_ERR_INVALID, "stream %d: n_q %d != the open chunk's %d tokens", sids[i],
+                    n_q, st->c_len[cur]);
+    }
+    const char* qi = static_cast<const char*>(q) + (size_t)q_off[i] * row_bytes;
+    char* oi = static_cast<char*>(out) + (size_t)q_off[i] * row_bytes;
+    if (pkv_status r = attend_args(h, st, qi, n_q, layer, oi, sm_scale, &calls[i])) return r;
+  }
+  // one launch (attention, then combine) per kernel shape; one split count each
+  std::vector<int> shape(n);
+  for (int i = 0; i < n; ++i) shape[i] = attend_tc_shape(calls[i].n_q);
+  size_t scratch = 0;
+  std::vector<int> splits_of_shape(4, 1);
+  for (int sh = 0; sh < 4; ++sh) {
+    int pairs = 0, max_tiles = 0;
+    for (int i = 0; i < n; ++i)
+      if (shape[i] == sh) {
+        pairs += attend_tc_mgroups(calls[i].n_q) * h->H;
+        max_tiles = std::max(max_tiles, calls[i].n_tiles);
+      }
+    if (pairs == 0) continue;
+    splits_of_shape[sh] = attend_tc_splits_pairs(pairs, max_tiles, h->num_sms);
+    for (int i = 0; i < n; ++i)
+      if (shape[i] == sh) {
+        calls[i].num_splits = splits_of_shape[sh];
+        if (calls[i].num_splits > 1) scratch += partial_bytes(calls[i]);
+      }
+  }
+  if (scratch > 0) {
+    if (pkv_status r = ensure_scratch(h, scratch)) return r;
+    float* base = h->d_scratch;
+    for (int i = 0; i < n; ++i)
+      if (calls[i].num_splits > 1) {
+        place_partials(&calls[i], base);
+        base += partial_bytes(calls[i]) / sizeof(float);
+      }
+  }
+  std::unique_ptr<AttendBatch> b(new AttendBatch);
+  for (int sh = 0; sh < 4; ++sh) {
+    std::memset(b.get(), 0, sizeof(AttendBatch));
+    for (int i = 0; i < n; ++i) {
+      if (shape[i] != sh) continue;
+      const int k = b->n++;
+      b->item[k] = calls[i];
+      b->n_mgroups[k] = attend_tc_mgroups(calls[i].n_q);
+      b->n_tiles[k] = calls[i].n_tiles;
+      b->cta_base[k + 1] = b->cta_base[k] + b->n_mgroups[k] * h->H * calls[i].num_splits;
+      b->pair_base[k + 1] = b->pair_base[k] + (long long)calls[i].n_q * h->H;
+    }
+    if (b->n > 0) PKV_CUDA(h, launch_attend_batch(*b, as_stream(cuda_stream)));
+  }
+  return PKV_OK;
 }
 
 pkv_status pkv_sync(pkv_t h, void* cuda_stream) {
@@ -952,50 +1043,23 @@ pkv_status pkv_attend_noalloc(pkv_t h, const void* q, int n_q, int sid, int laye
                               float sm_scale, void* cuda_stream) {
   Stream* st = nullptr;
   if (pkv_status r = get_stream(h, sid, &st)) return r;
-  if (!q || !out || !aligned16(q) || !aligned16(out))
-    return fail(h, PKV_ERR_INVALID, "q/out must be 16-byte aligned device pointers");
-  if (n_q < 1 || n_q > (1 << 20)) return fail(h, PKV_ERR_INVALID, "n_q %d out of range", n_q);
-  if (layer < 0 || layer >= h->L) return fail(h, PKV_ERR_INVALID, "layer %d out of range", layer);
   if (st->cfg.mode == PKV_MODE_CHUNKED) {
     if (!st->c_open) return fail(h, PKV_ERR_STATE, "no open chunk");
     const int cur = (st->c_head + st->n_chunks - 1) % st->cfg.sliding_window_num;
     if (n_q != st->c_len[cur])
       return fail(h, PKV_ERR_INVALID, "n_q %d != the open chunk's %d tokens", n_q, st->c_len[cur]);
   }
-  int np, nt, last;
-  visible_counts(h, *st, &np, &nt, &last);
-  if (nt == 0) return fail(h, PKV_ERR_STATE, "nothing is visible");
   AttendArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.q = static_cast<const uint16_t*>(q);
-  a.out = static_cast<uint16_t*>(out);
-  a.n_q = n_q;
-  a.heads = h->H;
-  a.pool = h->d_pool + (long long)layer * h->P * h->page_elems;
-  a.page_elems = h->page_elems;
-  a.page_size = h->Ps;
-  a.pool_pages = h->P;
-  a.tbl_idx = st->d_tbl_idx;
-  a.tbl_len = st->d_tbl_len;
-  a.tbl = table_args(h, *st, st->d_tbl_idx, st->d_tbl_len, nullptr, nullptr);
-  a.n_entries = np;
-  a.n_slots = (long long)(np - 1) * h->Ps + last;
-  a.n_tiles = ceil_div(a.n_slots, 64);
-  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)h->D);
-  a.scale_log2 = scale * 1.4426950408889634f;
+  if (pkv_status r = attend_args(h, st, q, n_q, layer, out, sm_scale, &a)) return r;
   a.num_splits = attend_num_splits(n_q, h->H, a.n_slots, h->num_sms);
-  a.err = h->d_err;
   if (a.num_splits > 1) {
-    const size_t o_bytes = (size_t)a.num_splits * n_q * h->H * kHeadDim * sizeof(float);
-    const size_t ml_bytes = (size_t)a.num_splits * n_q * h->H * 2 * sizeof(float);
-    if (o_bytes + ml_bytes > kStaticScratchBytes)
+    if (partial_bytes(a) > kStaticScratchBytes)
       return fail(h, PKV_ERR_INVALID,
                   "this call needs %zu bytes of split-KV scratch; the static scratch holds %zu",
-                  o_bytes + ml_bytes, kStaticScratchBytes);
+                  partial_bytes(a), kStaticScratchBytes);
     float* scratch = nullptr;
     if (pkv_status r = noalloc_scratch(h, &scratch)) return r;
-    a.part_o = scratch;
-    a.part_ml = scratch + o_bytes / sizeof(float);
+    place_partials(&a, scratch);
   }
   cudaStream_t s = as_stream(cuda_stream);
   PKV_CUDA(h, launch_attend(a, h->num_sms, s));

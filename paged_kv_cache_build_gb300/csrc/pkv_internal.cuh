@@ -202,6 +202,18 @@ struct AttendArgs {
   int* err;
 };
 
+// Several attention calls in one launch (streams of one kernel shape). Item i
+// owns CTAs cta_base[i] .. cta_base[i+1] - 1 of the attention kernel and
+// (query row, head) pairs pair_base[i] .. pair_base[i+1] - 1 of the combine.
+struct AttendBatch {
+  int n;
+  int cta_base[kMaxBatch + 1];
+  long long pair_base[kMaxBatch + 1];
+  int n_mgroups[kMaxBatch];
+  int n_tiles[kMaxBatch];
+  AttendArgs item[kMaxBatch];
+};
+
 // Kernel launches made by this library in this process (every launcher counts).
 // ---------------------------------------------------- dependent launches
 // The frame path's kernels are launched with programmatic stream serialization:
@@ -246,6 +258,15 @@ cudaError_t launch_table(const TableArgs& a, cudaStream_t s);
 cudaError_t launch_attend(const AttendArgs& a, int num_sms, cudaStream_t s);
 int attend_num_splits(int n_q, int heads, long long n_slots, int num_sms);
 cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t s);
+// A batch whose items share one kernel shape (attend_tc_shape of their n_q),
+// with the attention and, for splits > 1, the combine.
+cudaError_t launch_attend_batch(const AttendBatch& b, cudaStream_t s);
+cudaError_t launch_attend_tc_batch(const AttendBatch& b, cudaStream_t s);
+int attend_tc_shape(int n_q);                  // kernel shape (M-tiles, extra rows): 0 .. 3
+int attend_tc_mgroups(int n_q);
+// Split-KV factor for `pairs` (M-group, head) pairs whose longest table has
+// n_tiles tiles: fill the SMs in as few, as even waves as possible.
+int attend_tc_splits_pairs(int pairs, int n_tiles, int num_sms);
 int attend_tc_splits(int n_q, int heads, int n_tiles, int num_sms);
 int attend_tc_tiles(long long n_slots);
 cudaError_t launch_synth(uint16_t* dst, int n_frames, int n_tokens, int heads, int head_dim,
