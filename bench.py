@@ -535,8 +535,6 @@ def run_ours(args):
         cache.sync()
 
     # ---- main timed region
-    launches0 = kernel_launches()
-    per_step_launches = None
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()

@@ -760,8 +760,6 @@ static pkv_status attend_args(pkv_t h, Stream* st, const void* q, int n_q, int l
   a->page_elems = h->page_elems;
   a->page_size = h->Ps;
   a->pool_pages = h->P;
-  a->tbl_idx = st->d_tbl_idx;
-  a->tbl_len = st->d_tbl_len;
   a->tbl = table_args(h, *st, st->d_tbl_idx, st->d_tbl_len, nullptr, nullptr);
   a->n_entries = np;
   a->n_slots = (long long)(np - 1) * h->Ps + last;

@@ -189,9 +189,7 @@ struct AttendArgs {
   long long page_elems;
   int page_size;
   int pool_pages;
-  const int32_t* tbl_idx;            // visible table (read by the mma.sync kernel)
-  const int32_t* tbl_len;
-  TableArgs tbl;                     // the same table, computed on the fly by the producer
+  TableArgs tbl;                     // the visible table, computed on the fly by the producer
   int n_entries;
   int n_tiles;                      // 64-slot tiles covering the table's slots
   long long n_slots;                // flat slots up to the last valid one
