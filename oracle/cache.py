@@ -372,6 +372,18 @@ class PagedCacheOracle:
             out.extend(self.slots[p][:n])
         return out
 
+    def visible_tokens_sampled(self, sid, seed, layer, keep):
+        """Provenance of the visible tokens of the pages a layer keeps under the
+        per-layer random subset (oracle/sampling.py): frame mode, scale pages
+        always kept."""
+        from .sampling import kept_positions
+        st = self._stream(sid, "frame")
+        idx, lens = self.visible_table(sid)
+        out = []
+        for e in kept_positions(len(idx), len(st.scale), seed, layer, keep):
+            out.extend(self.slots[idx[e]][:lens[e]])
+        return out
+
     def snapshot(self, sid=None):
         """Metadata and the provenance of every valid slot, for identity checks."""
         snap = {"free": list(self.free), "streams": {}}
