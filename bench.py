@@ -464,6 +464,48 @@ def extra_multistream(frames=100, reps=20):
             "attn_tflops_batched": round(flops / (res["batched"] * 1e-3) / 1e12, 2)}
 
 
+def extra_sampled(frames=150, reps=20):
+    """A steady-state LingBot-shaped frame (one layer) attending to a random
+    subset of its visible pages (pkv_attend_sampled): us per call at keep 1,
+    1/2 and 1/4 of the pages (scale pages always kept)."""
+    import torch
+    from paged_kv_cache_build_gb300 import PagedKVCache, frame_stream_cfg, synth_fill
+    from synth import TENSOR_K, TENSOR_Q, TENSOR_V, WORKLOADS
+    w = WORKLOADS["lingbot"]
+    T, H, D = w.frame_tokens, w.heads, w.head_dim
+    cache = PagedKVCache(w.pool_pages, w.page_size, H, D)
+    sid = cache.open_stream(frame_stream_cfg(w.num_scale, w.window, w.n_patch, w.n_special))
+    kv = torch.empty((2, 8, T, H, D), dtype=torch.bfloat16, device="cuda")
+    synth_fill(kv[0], 0, w.index, 0, 0, 0, TENSOR_K)
+    synth_fill(kv[1], 0, w.index, 0, 0, 0, TENSOR_V)
+    for t in range(frames):
+        cache.append_frame(sid, kv[0, t % 8], kv[1, t % 8])
+        if t < frames - 1:
+            cache.evict_window(sid)
+    q = torch.empty((T, H, D), dtype=torch.bfloat16, device="cuda")
+    synth_fill(q, 0, w.index, 0, 0, 0, TENSOR_Q, 0, w.q_scale)
+    out = torch.empty_like(q)
+    res = {}
+    for keep in (65536, 32768, 16384):
+        times = []
+        for r in range(reps + 3):
+            e0, e1 = _events()
+            torch.cuda._sleep(HOST_COVER_CYCLES)
+            e0.record()
+            cache.attend_sampled(q, sid, 0, seed=r, keep=keep, out=out, sm_scale=w.sm_scale)
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 3:
+                times.append(e0.elapsed_time(e1))
+        res[keep] = statistics.median(times) * 1e3
+    cache.sync()
+    cache.close()
+    return {"workload": "lingbot frame %d, one layer, seeds 3..%d" % (frames - 1, reps + 2),
+            "us_keep_all": round(res[65536], 2), "us_keep_half": round(res[32768], 2),
+            "us_keep_quarter": round(res[16384], 2),
+            "speedup_quarter": round(res[65536] / res[16384], 2)}
+
+
 # ------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -671,7 +713,7 @@ def run_ours(args):
     }
     if not args.no_extra:
         line["extra"] = {"chunked": extra_chunked(), "long24": extra_long24(), "append": extra_append(),
-                         "multistream": extra_multistream()}
+                         "multistream": extra_multistream(), "sampled": extra_sampled()}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)

@@ -191,6 +191,25 @@ pkv_status pkv_attend(pkv_t h, const void* q, int n_q, int stream_id, int layer,
 pkv_status pkv_attend_chunked(pkv_t h, const void* q, int n_q, int stream_id, int layer,
                               void* out, float sm_scale, void* cuda_stream);
 
+/* Frame-mode attention over a per-layer random subset of the visible pages.
+ * vLLM-Omni RFC "Reconstruction Engine", section 5 (KV compression): AVGGT
+ * samples a random KV subset per layer, different layers drawing different
+ * subsets; FastVGGT keeps the initial frames as global anchors. Read at page
+ * granularity on the visible table of "LingBot-Map Paged KV Cache", section 2:
+ * the scale pages are always kept; the page at table position e (0-based, in
+ * the order scale -> window -> special) is otherwise kept when the low 16 bits
+ * of splitmix64(seed XOR (layer << 32) XOR e) are below keep, so each page is
+ * kept with probability keep / 65536. splitmix64(x) is the first output of the
+ * published generator seeded with x: z = x + 0x9E3779B97F4A7C15, then
+ * z ^= z >> 30, z *= 0xBF58476D1CE4E5B9, z ^= z >> 27, z *= 0x94D049BB133111EB,
+ * z ^= z >> 31. The attention is pkv_attend's over the kept pages' valid slots.
+ * keep: 0 .. 65536 (65536 keeps every page). Errors: as pkv_attend; STATE for
+ * a chunked-mode stream or an empty subset; INVALID for more than 1024 visible
+ * pages. */
+pkv_status pkv_attend_sampled(pkv_t h, const void* q, int n_q, int stream_id, int layer, void* out,
+                              float sm_scale, unsigned long long seed, int keep,
+                              void* cuda_stream);
+
 /* Several streams' attention in one launch (the multi-stream pool of LingBot-Map
  * section 4; batching in the manner of the vLLM-Omni RFC's scheduler, section
  * 2.3). Equivalent to n calls of pkv_attend (frame-mode streams) or

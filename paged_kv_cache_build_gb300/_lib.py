@@ -38,6 +38,8 @@ SIGNATURES = {
     "pkv_attend": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_float, c_void_p]),
     "pkv_attend_chunked": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_float,
                                    c_void_p]),
+    "pkv_attend_sampled": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_float,
+                                   ctypes.c_ulonglong, c_int, c_void_p]),
     "pkv_attend_batched": (c_int, [c_void_p, c_void_p, ctypes.POINTER(c_int), ctypes.POINTER(c_int),
                                    c_int, c_int, c_void_p, c_float, c_void_p]),
     "pkv_attend_noalloc": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_float,

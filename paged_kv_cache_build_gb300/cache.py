@@ -122,6 +122,17 @@ class PagedKVCache:
                                                 _stream_ptr(stream)))
         return out
 
+    def attend_sampled(self, q, sid, layer=0, seed=0, keep=65536, out=None, sm_scale=0.0, stream=None):
+        """pkv_attend_sampled: attention over a per-layer random subset of the
+        visible pages (scale pages always kept, others with probability
+        keep / 65536)."""
+        if out is None:
+            out = torch.empty_like(q)
+        self._check(self.lib.pkv_attend_sampled(self.h, _bf16_ptr(q, "q"), q.shape[0], sid, layer,
+                                                _bf16_ptr(out, "out"), float(sm_scale), int(seed),
+                                                int(keep), _stream_ptr(stream)))
+        return out
+
     def attend_batched(self, qs, sids, layer=0, sm_scale=0.0, stream=None):
         """pkv_attend_batched: the streams' attention in one launch. qs: one
         [n_q][heads][64] bf16 tensor per stream (packed into one buffer here);

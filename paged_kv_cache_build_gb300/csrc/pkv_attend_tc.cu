@@ -68,6 +68,7 @@ struct __align__(1024) TcSmem {
   float xo[kXWarps][kXRows][kHeadDim];  // extra rows: each warp's partial O ...
   float xml[kXWarps][kXRows][2];        // ... and its running max and sum
   uint64_t mask[kStages];            // slot validity of the stage's tile
+  uint16_t kept[kMaxSampledEntries]; // a sampled call's kept table positions
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[MT][2];            // S_m of the buffer's latest tile is in TMEM
@@ -360,10 +361,26 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   }
   // Visible-table entries for the producer, 32 at a time (one per lane): the
   // entry lookups are dependent global loads, so a batch costs one latency.
+  // A sampled call's kept table positions, in order (producer warp, a ballot
+  // per 32 positions); the producer then indexes the kept pages only.
+  if (warp == kProducerWarp && a.sampled) {
+    int count = 0;
+    for (int e0 = 0; e0 < a.n_entries_all; e0 += 32) {
+      const int e = e0 + lane;
+      const bool keep = e < a.n_entries_all &&
+                        (e < a.sample_anchor || page_sample_kept(a.sample_key, e, a.sample_keep));
+      const unsigned ball = __ballot_sync(0xffffffffu, keep);
+      if (keep) sm.kept[count + __popc(ball & ((1u << lane) - 1u))] = (uint16_t)e;
+      count += __popc(ball);
+    }
+    __syncwarp();
+  }
+  // table position of the producer's e-th entry
+  auto entry_of = [&](int e) { return a.sampled ? (int)sm.kept[e] : e; };
   const int e_first = (int)((long long)t0 * kBN / Ps);
   int e_batch = e_first & ~31, e_page = 0, e_len = 0;
   if (warp == kProducerWarp && e_batch + lane < a.n_entries)
-    table_entry(a.tbl, e_batch + lane, e_page, e_len);
+    table_entry(a.tbl, entry_of(e_batch + lane), e_page, e_len);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -392,7 +409,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
         if ((e & ~31) != e_batch) {                // warp-uniform: next batch of entries
           e_batch = e & ~31;
           e_page = e_len = 0;
-          if (e_batch + lane < a.n_entries) table_entry(a.tbl, e_batch + lane, e_page, e_len);
+          if (e_batch + lane < a.n_entries) table_entry(a.tbl, entry_of(e_batch + lane), e_page, e_len);
         }
         const int page = __shfl_sync(0xffffffffu, e_page, e - e_batch);
         const int len = __shfl_sync(0xffffffffu, e_len, e - e_batch);

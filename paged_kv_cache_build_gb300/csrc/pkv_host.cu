@@ -816,6 +816,48 @@ pkv_status pkv_attend_chunked(pkv_t h, const void* q, int n_q, int sid, int laye
   return attend_common(h, st, q, n_q, layer, out, sm_scale, as_stream(cuda_stream));
 }
 
+pkv_status pkv_attend_sampled(pkv_t h, const void* q, int n_q, int sid, int layer, void* out,
+                              float sm_scale, unsigned long long seed, int keep, void* cuda_stream) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  if (st->cfg.mode != PKV_MODE_FRAME)
+    return fail(h, PKV_ERR_STATE, "pkv_attend_sampled needs a frame-mode stream");
+  if (keep < 0 || keep > 65536) return fail(h, PKV_ERR_INVALID, "keep %d outside 0..65536", keep);
+  AttendArgs a;
+  if (pkv_status r = attend_args(h, st, q, n_q, layer, out, sm_scale, &a)) return r;
+  const int np = a.n_entries;
+  if (np > kMaxSampledEntries)
+    return fail(h, PKV_ERR_INVALID, "%d visible pages; a sampled call takes at most %d", np,
+                kMaxSampledEntries);
+  // the same decisions the kernel's producer makes, to size the grid: the
+  // kept pages and the length of the last one
+  const TableArgs& t = a.tbl;
+  const unsigned long long key = seed ^ ((unsigned long long)layer << 32);
+  int n_kept = 0, last_len = 0;
+  for (int e = 0; e < np; ++e) {
+    if (e >= t.n_scale && !page_sample_kept(key, e, keep)) continue;
+    ++n_kept;
+    const int k = e - t.n_scale - t.win_count;          // special page index, if >= 0
+    last_len = k < 0 ? h->Ps : (k == t.n_special - 1 ? t.sp_last_len : t.sp_full_len);
+  }
+  if (n_kept == 0) return fail(h, PKV_ERR_STATE, "the sampled subset of the visible pages is empty");
+  a.sampled = 1;
+  a.sample_keep = keep;
+  a.sample_anchor = t.n_scale;
+  a.sample_key = key;
+  a.n_entries_all = np;
+  a.n_entries = n_kept;
+  a.n_slots = (long long)(n_kept - 1) * h->Ps + last_len;
+  a.n_tiles = ceil_div(a.n_slots, 64);
+  a.num_splits = attend_num_splits(n_q, h->H, a.n_slots, h->num_sms);
+  if (a.num_splits > 1) {
+    if (pkv_status r = ensure_scratch(h, partial_bytes(a))) return r;
+    place_partials(&a, h->d_scratch);
+  }
+  PKV_CUDA(h, launch_attend(a, h->num_sms, as_stream(cuda_stream)));
+  return PKV_OK;
+}
+
 pkv_status pkv_attend_batched(pkv_t h, const void* q, const int* q_off, const int* sids, int n,
                               int layer, void* out, float sm_scale, void* cuda_stream) {
   if (!h) return fail(h, PKV_ERR_INVALID, "null handle");

@@ -190,6 +190,15 @@ struct AttendArgs {
   int page_size;
   int pool_pages;
   TableArgs tbl;                     // the visible table, computed on the fly by the producer
+  // Per-layer random page subset (pkv_attend_sampled; sampled = 0 attends to
+  // every visible page): the first sample_anchor table positions are kept, any
+  // other position e when page_sample_kept(sample_key, e, sample_keep). Then
+  // n_entries counts the kept pages and n_entries_all every visible one.
+  int sampled;
+  int sample_keep;
+  int sample_anchor;
+  int n_entries_all;
+  unsigned long long sample_key;
   int n_entries;
   int n_tiles;                      // 64-slot tiles covering the table's slots
   long long n_slots;                // flat slots up to the last valid one
@@ -211,6 +220,22 @@ struct AttendBatch {
   int n_tiles[kMaxBatch];
   AttendArgs item[kMaxBatch];
 };
+
+// ------------------------------------------------------- page sampling
+// vLLM-Omni RFC "Reconstruction Engine", section 5 (KV compression: AVGGT draws
+// a random KV subset per layer): a non-anchor page at table position e is kept
+// when the low 16 bits of splitmix64(key XOR e) are below keep (a fraction in
+// 1/65536 units), key = seed XOR (layer << 32). splitmix64 as published by
+// Steele, Lea and Flood (OOPSLA 2014): the state advances by the golden gamma,
+// then is mixed.
+constexpr int kMaxSampledEntries = 1024;   // visible pages a sampled call may hold
+__host__ __device__ inline bool page_sample_kept(unsigned long long key, int e, int keep) {
+  unsigned long long z = (key ^ (unsigned long long)e) + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  return (int)(z & 0xFFFFull) < keep;
+}
 
 // Kernel launches made by this library in this process (every launcher counts).
 // ---------------------------------------------------- dependent launches
