@@ -19,7 +19,10 @@ Sources (page title, section):
   * vLLM-Omni RFC "Reconstruction Engine" (issue 2727), section 2.3
     (sequence_length = sliding_window_num x chunk_size) and section 3.3
     (executor chunk loop: global attention over in-window KV plus the
-    current chunk, KV append, evict the oldest chunk).
+    current chunk, KV append, evict the oldest chunk); section 2.2 and 3.3
+    (frame attention, each frame's tokens over that frame's own tokens,
+    alternating with the global attention); section 5 (KV compression: the
+    per-layer random page subset of sampling.py).
 
 Parity of every function here is pinned in tests/test_oracle_*.py against a
 brute-force flat model, closed forms, a library softmax-attention routine and
@@ -27,4 +30,4 @@ a hand-derived page trace (tests/golden/).
 """
 
 from .cache import OracleError, PagedCacheOracle, StreamConfig  # noqa: F401
-from .attention import attend_fp64, gather_visible  # noqa: F401
+from .attention import attend_fp64, frame_attend_fp64, gather_visible  # noqa: F401

@@ -72,6 +72,29 @@ def attend_fp64(q_bits, k_bits, v_bits, sm_scale, rows=None):
     return out
 
 
+def frame_attend_fp64(q_bits, k_bits, v_bits, sm_scale):
+    """Intra-frame attention in fp64.
+
+    vLLM-Omni RFC "Reconstruction Engine", section 2.2: VGGT's aggregator
+    alternates frame self-attention with global self-attention; section 3.3: the
+    worker runs frame attention per frame before the global attention. Frame
+    attention is read as the plain softmax attention of each frame's tokens over
+    that frame's own tokens (bidirectional, no cache):
+        out[f] = attend_fp64(q[f], k[f], v[f]) for every frame f.
+    q_bits, k_bits, v_bits: bf16 bits [n_frames][tokens][H][D].
+    Returns fp64 [n_frames][tokens][H][D].
+    """
+    q = np.asarray(q_bits, dtype=np.uint16)
+    k = np.asarray(k_bits, dtype=np.uint16)
+    v = np.asarray(v_bits, dtype=np.uint16)
+    if q.ndim != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share the shape [n_frames][tokens][heads][head_dim]")
+    out = np.empty(q.shape, dtype=np.float64)
+    for f in range(q.shape[0]):
+        out[f] = attend_fp64(q[f], k[f], v[f], sm_scale)
+    return out
+
+
 def softmax_rows_fp64(q_bits, k_bits, sm_scale, head):
     """The softmax probability rows of one head (for row-sum checks)."""
     q = _widen(q_bits)[:, head, :]
