@@ -311,10 +311,49 @@ def extra_chunked(reps=5):
             "ms_per_chunk": round(ms, 4), "attn_tflops": round(flops / (ms * 1e-3) / 1e12, 2)}
 
 
-def extra_long24(frames=240, warm=100):
+def extra_frames(reps=20, reps_small=200):
+    """Intra-frame attention (pkv_attend_frames), 16 heads x 64: a VGGT chunk's 8
+    frames of 1,374 tokens in one call (TFLOP/s), and one LingBot-Map frame of 262
+    tokens (us per call, calls back to back)."""
+    import torch
+    from paged_kv_cache_build_gb300 import PagedKVCache, synth_fill
+    from synth import TENSOR_K, TENSOR_Q, TENSOR_V, WORKLOADS
+    res = {}
+    for name, w, F in (("vggt_chunk", WORKLOADS["chunked"], WORKLOADS["chunked"].chunk_size),
+                       ("lingbot_frame", WORKLOADS["lingbot"], 1)):
+        T = w.frame_tokens
+        cache = PagedKVCache(4, 16, w.heads)
+        x = torch.empty((3, F, T, w.heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+        synth_fill(x[0], 0, w.index, 0, 0, 0, TENSOR_Q, 0, w.q_scale)
+        synth_fill(x[1], 0, w.index, 0, 0, 0, TENSOR_K)
+        synth_fill(x[2], 0, w.index, 0, 0, 0, TENSOR_V)
+        out = torch.empty_like(x[0])
+        n = reps if F > 1 else reps_small
+        for _ in range(3):
+            cache.attend_frames(x[0], x[1], x[2], out=out, sm_scale=w.sm_scale)
+        torch.cuda.synchronize()
+        e0, e1 = _events()
+        e0.record()
+        for _ in range(n):
+            cache.attend_frames(x[0], x[1], x[2], out=out, sm_scale=w.sm_scale)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        flops = 4.0 * F * T * T * w.head_dim * w.heads
+        res[name] = {"frames": F, "tokens": T, "us_per_call": round(ms * 1e3, 2),
+                     "attn_tflops": round(flops / (ms * 1e-3) / 1e12, 2)}
+        cache.sync()
+        cache.close()
+    return res
+
+
+def extra_long24(frames=240, warm=100, frame_attn=False):
     """The 24-layer keyframe stream (kf 4): per frame, for each layer, append and
     attend; then evict (keyframe) or roll back. frame-steps/s over `frames` frames
-    after `warm` frames (inputs from a ring of 8 frames per layer)."""
+    after `warm` frames (inputs from a ring of 8 frames per layer). With
+    frame_attn, each layer first runs the frame's intra-frame attention
+    (pkv_attend_frames), the model-shaped step of frame attention alternating
+    with global attention; its q/k/v are the ring's next slot."""
     import torch
     from paged_kv_cache_build_gb300 import PagedKVCache, frame_stream_cfg, synth_fill
     from synth import TENSOR_K, TENSOR_Q, TENSOR_V, WORKLOADS, is_keyframe
@@ -331,8 +370,14 @@ def extra_long24(frames=240, warm=100):
         synth_fill(v[layer], 0, w.index, sid, layer, 0, TENSOR_V)
         synth_fill(q[layer], 0, w.index, sid, layer, 0, TENSOR_Q, 0, w.q_scale)
 
+    out_f = torch.empty_like(out)
+
     def frame(t):
         for layer in range(L):
+            if frame_attn:
+                u = (t + 1) % R
+                cache.attend_frames(q[layer, u], k[layer, u], v[layer, u], out=out_f,
+                                    sm_scale=w.sm_scale)
             cache.append_frame(sid, k[layer, t % R], v[layer, t % R], layer)
             cache.attend(q[layer, t % R], sid, layer, out=out, sm_scale=w.sm_scale)
         if is_keyframe(t, w.num_scale, w.keyframe_interval):
@@ -352,7 +397,8 @@ def extra_long24(frames=240, warm=100):
     ms = e0.elapsed_time(e1)
     cache.sync()
     cache.close()
-    return {"workload": "long-24layer-kf4 (frames %d-%d, eager calls)" % (warm, warm + frames - 1),
+    name = "model-24layer-kf4, frame + global attention" if frame_attn else "long-24layer-kf4"
+    return {"workload": "%s (frames %d-%d, eager calls)" % (name, warm, warm + frames - 1),
             "frame_steps_per_s": round(frames / (ms * 1e-3), 2),
             "ms_per_frame_step": round(ms / frames, 4)}
 
@@ -713,7 +759,8 @@ def run_ours(args):
     }
     if not args.no_extra:
         line["extra"] = {"chunked": extra_chunked(), "long24": extra_long24(), "append": extra_append(),
-                         "multistream": extra_multistream(), "sampled": extra_sampled()}
+                         "multistream": extra_multistream(), "sampled": extra_sampled(),
+                         "frames": extra_frames(), "model24": extra_long24(frame_attn=True)}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)

@@ -210,6 +210,25 @@ pkv_status pkv_attend_sampled(pkv_t h, const void* q, int n_q, int stream_id, in
                               float sm_scale, unsigned long long seed, int keep,
                               void* cuda_stream);
 
+/* Intra-frame attention: the tokens of every frame attend to that frame's own
+ * tokens only, bidirectionally; no page, stream or table of the cache is read or
+ * changed. vLLM-Omni RFC "Reconstruction Engine", section 2.2 (VGGT's aggregator
+ * alternates frame self-attention with global self-attention in each of its 24
+ * layers) and section 3.3 (the worker runs frame attention, per frame, before the
+ * global attention over the in-window KV). For every frame f < n_frames, query
+ * row i < tokens and head h:
+ *   out[f][i][h] = softmax(sm_scale * q[f][i][h] . k[f][:][h]^T) v[f][:][h].
+ * q, k, v, out: device bf16 [n_frames][tokens][heads][64], contiguous, each
+ * 16-byte aligned (heads = the handle's); the caller owns them; out is written,
+ * nothing else. fp32 accumulation and softmax, as pkv_attend; sm_scale <= 0
+ * means 1/sqrt(head_dim). K and V are read by the Tensor Memory Accelerator
+ * through tensor maps built by the driver's cuTensorMapEncodeTiled for each call.
+ * n_frames = 0 is a no-op. Errors: INVALID for a null handle or pointer, an
+ * unaligned pointer, tokens outside 1 .. 2^20, n_frames < 0, or n_frames x tokens
+ * above 2^31 - 65; CUDA if the tensor maps cannot be built or the launch fails. */
+pkv_status pkv_attend_frames(pkv_t h, const void* q, const void* k, const void* v, int n_frames,
+                             int tokens, void* out, float sm_scale, void* cuda_stream);
+
 /* Several streams' attention in one launch (the multi-stream pool of LingBot-Map
  * section 4; batching in the manner of the vLLM-Omni RFC's scheduler, section
  * 2.3). Equivalent to n calls of pkv_attend (frame-mode streams) or

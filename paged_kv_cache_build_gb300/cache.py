@@ -152,6 +152,25 @@ class PagedKVCache:
                                                 _stream_ptr(stream)))
         return [out[off[i]:off[i + 1]] for i in range(n)]
 
+    def attend_frames(self, q, k, v, out=None, sm_scale=0.0, stream=None):
+        """pkv_attend_frames: intra-frame attention, each frame's tokens over
+        that frame's own tokens. q, k, v: [n_frames][tokens][heads][64] (or one
+        frame, [tokens][heads][64]) contiguous bf16 CUDA tensors."""
+        if q.shape != k.shape or q.shape != v.shape:
+            raise ValueError("q, k and v must have the same shape")
+        if q.dim() not in (3, 4):
+            raise ValueError("expected [n_frames][tokens][heads][64] or [tokens][heads][64]")
+        if tuple(q.shape[-2:]) != (self.heads, self.head_dim):
+            raise ValueError(f"rows must be [{self.heads}][{self.head_dim}]")
+        n_frames, tokens = (1, q.shape[0]) if q.dim() == 3 else (q.shape[0], q.shape[1])
+        if out is None:
+            out = torch.empty_like(q)
+        self._check(self.lib.pkv_attend_frames(self.h, _bf16_ptr(q, "q"), _bf16_ptr(k, "k"),
+                                               _bf16_ptr(v, "v"), n_frames, tokens,
+                                               _bf16_ptr(out, "out"), float(sm_scale),
+                                               _stream_ptr(stream)))
+        return out
+
     def attend_noalloc(self, q, sid, layer=0, out=None, sm_scale=0.0, stream=None):
         """pkv_attend_noalloc: attention whose scratch is a fixed device array."""
         if out is None:

@@ -4,7 +4,10 @@
 // valid slot of the visible pages (scale -> window -> special, the frame's own
 // tokens included), bidirectionally, masked only by each page's valid length.
 // vLLM-Omni RFC "Reconstruction Engine", section 3.3: a chunk's tokens attend over
-// the in-window chunks the same way.
+// the in-window chunks the same way. The same RFC, sections 2.2 and 3.3: frame
+// attention, each frame's tokens attending to their own frame only, alternates
+// with the global attention; here the keys and values are the frame's dense
+// [tokens][heads][64] tensors, read by TMA through tensor maps.
 //
 // One CTA computes, for one head, MT (1 or 2) M-tiles of 128 query rows, plus
 // up to 8 extra rows, against a range of 64-slot KV tiles of the visible table
@@ -14,7 +17,10 @@
 //                tile into an 8-stage shared-memory ring, plus the tile's 64-bit
 //                slot-validity mask. Pages are stored in the pool already
 //                128-byte swizzled, so a block lands in shared memory as a ready
-//                tensor-core operand; no tensor map is needed.
+//                tensor-core operand; no tensor map is needed. Frame attention
+//                instead loads each 64-token K and V tile with one 3-D tensor
+//                copy (cp.async.bulk.tensor) whose 128-byte swizzle gives the
+//                same operand layout.
 //   warps 3, 1   MMA issuers (one thread each, one per M-tile): S_m = Q_m K^T
 //                (N = 64 slots) into one of two TMEM buffers, and O_m += P_m V
 //                with P_m read from one of two TMEM buffers.
@@ -35,6 +41,8 @@
 // error word, and the CTA drains its copies and MMAs and frees TMEM before
 // returning.
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "pkv_internal.cuh"
 
@@ -185,6 +193,17 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
       : "memory");
 }
 
+// One box of a 3-D tensor map (coordinates innermost first) into shared memory,
+// completing on `mbar` with the box's bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(mbar)
+      : "memory");
+}
+
 #define PKV_TMEM_LD16(taddr, r)                                                                  \
   asm volatile(                                                                                  \
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"   \
@@ -279,18 +298,24 @@ constexpr int kProducerWarp = 2;
 constexpr int kMmaWarp = 3;          // MMA issuer of M-tile 0 (and TMEM owner)
 constexpr int kMmaWarp2 = 1;         // MMA issuer of M-tile 1
 
-// The call a CTA works on: the launch's only one, or its stream's in a batch.
+// The call a CTA works on: the launch's only one, or its stream's in a batch,
+// or (frame attention) its frame.
 struct CtaWork {
   const AttendArgs* a;
   int bid, n_mgroups, n_tiles;
+  int frame;                        // frame attention: the CTA's frame; else 0
 };
 __device__ __forceinline__ CtaWork cta_work(const AttendArgs& a, int n_mgroups, int n_tiles) {
-  return {&a, (int)blockIdx.x, n_mgroups, n_tiles};
+  return {&a, (int)blockIdx.x, n_mgroups, n_tiles, 0};
 }
 __device__ __forceinline__ CtaWork cta_work(const AttendBatch& b, int, int) {
   int i = 0;
   while (i + 1 < b.n && (int)blockIdx.x >= b.cta_base[i + 1]) ++i;
-  return {&b.item[i], (int)blockIdx.x - b.cta_base[i], b.n_mgroups[i], b.n_tiles[i]};
+  return {&b.item[i], (int)blockIdx.x - b.cta_base[i], b.n_mgroups[i], b.n_tiles[i], 0};
+}
+__device__ __forceinline__ CtaWork cta_work(const AttendDense& d, int n_mgroups, int n_tiles) {
+  const int per_frame = n_mgroups * d.a.heads;
+  return {&d.a, (int)blockIdx.x % per_frame, n_mgroups, n_tiles, (int)blockIdx.x / per_frame};
 }
 
 template <int MT, bool EXTRA, typename Params>
@@ -304,6 +329,11 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   const AttendArgs& a = *cw.a;
   const int n_mgroups = cw.n_mgroups, n_tiles = cw.n_tiles;
   const int H = a.heads, Ps = a.page_size;
+  constexpr bool kDense = std::is_same<Params, AttendDense>::value;
+  // this CTA's query and output rows (a frame's, in frame attention)
+  const long long row_base = (long long)cw.frame * a.n_q;
+  const uint16_t* const qg = a.q + row_base * H * kHeadDim;
+  uint16_t* const og = a.out + row_base * H * kHeadDim;
 
   int bid = cw.bid;
   const int mg = bid % n_mgroups;
@@ -354,7 +384,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
       const int row = row0 + m * 128 + r;
       uint4 val = make_uint4(0u, 0u, 0u, 0u);
       if (row < a.n_q)
-        val = __ldg(reinterpret_cast<const uint4*>(a.q + ((long long)row * H + h) * kHeadDim + c * 8));
+        val = __ldg(reinterpret_cast<const uint4*>(qg + ((long long)row * H + h) * kHeadDim + c * 8));
       *reinterpret_cast<uint4*>(&sm.q[m][r * 128 + (swizzle_chunk(r, c) << 4)]) = val;
     }
     fence_proxy_async();
@@ -377,7 +407,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   }
   // table position of the producer's e-th entry
   auto entry_of = [&](int e) { return a.sampled ? (int)sm.kept[e] : e; };
-  const int e_first = (int)((long long)t0 * kBN / Ps);
+  const int e_first = kDense ? 0 : (int)((long long)t0 * kBN / Ps);
   int e_batch = e_first & ~31, e_page = 0, e_len = 0;
   if (warp == kProducerWarp && e_batch + lane < a.n_entries)
     table_entry(a.tbl, entry_of(e_batch + lane), e_page, e_len);
@@ -392,9 +422,30 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     // The whole warp walks the tiles (its lanes hold the cached table entries);
     // lane 0 issues the copies.
     int issued_tiles = 0;
+    if constexpr (kDense) {
+      // frame attention: tile t is tokens 64 t .. 64 t + 63 of the CTA's frame,
+      // one K and one V box of head h; the slots past the frame's last token
+      // (the next frame's, or the tensor map's zero fill after the last frame)
+      // are masked
+      const int kv_row0 = cw.frame * a.n_q;
+      for (int j = 0; j < nT; ++j) {
+        const int s = j % kStages;
+        if (!mbar_wait(&sm.kv_empty[s], ((j / kStages) & 1) ^ 1, abort, a.err)) break;
+        const int tile = t0 + j;
+        const int n = min(kBN, a.n_q - tile * kBN);  // >= 1: tile < n_tiles
+        if (lane == 0) {
+          sm.mask[s] = n >= kBN ? ~0ull : ((1ull << n) - 1ull);
+          const uint32_t mb = smem_u32(&sm.kv_full[s]);
+          mbar_arrive_expect_tx(&sm.kv_full[s], 2u * kBN * 128u);
+          tma_load_3d(smem_u32(&sm.k[s][0]), &params.k_map, 0, h, kv_row0 + tile * kBN, mb);
+          tma_load_3d(smem_u32(&sm.v[s][0]), &params.v_map, 0, h, kv_row0 + tile * kBN, mb);
+        }
+        issued_tiles = j + 1;
+      }
+    }
     const int per = Ps >= kBN ? 1 : kBN / Ps;      // page blocks per tile
     const int rows = Ps >= kBN ? kBN : Ps;         // slots per block
-    for (int j = 0; j < nT; ++j) {
+    for (int j = 0; !kDense && j < nT; ++j) {
       const int s = j % kStages;
       if (!mbar_wait(&sm.kv_empty[s], ((j / kStages) & 1) ^ 1, abort, a.err)) break;
       const int tile = t0 + j;
@@ -654,7 +705,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     }
     if (write) {
       if (a.num_splits == 1) {
-        uint4* dst = reinterpret_cast<uint4*>(a.out + ((long long)row * H + h) * kHeadDim);
+        uint4* dst = reinterpret_cast<uint4*>(og + ((long long)row * H + h) * kHeadDim);
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
           const float* f = reinterpret_cast<const float*>(&o[8 * q4]);
@@ -691,7 +742,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
 #pragma unroll
         for (int i = 0; i < 2; ++i)
           qb[kk][i] = qrow < a.n_q ? __ldg(reinterpret_cast<const uint32_t*>(
-                                         a.q + ((long long)qrow * H + h) * kHeadDim + kk * 16 +
+                                         qg + ((long long)qrow * H + h) * kHeadDim + kk * 16 +
                                          i * 8 + 2 * tq))
                                    : 0u;
     }
@@ -813,7 +864,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
 #pragma unroll
             for (int i = 0; i < kXWarps; ++i) val += w[i] * sm.xo[i][xq][d];
             if (a.num_splits == 1)
-              a.out[((long long)xrow * H + h) * kHeadDim + d] =
+              og[((long long)xrow * H + h) * kHeadDim + d] =
                   __bfloat16_as_ushort(__float2bfloat16_rn(val * inv));
             else
               a.part_o[ro * kHeadDim + d] = val;
@@ -920,6 +971,12 @@ cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t s) {
 
 cudaError_t launch_attend_tc_batch(const AttendBatch& b, cudaStream_t s) {
   return launch_shape(attend_tc_shape(b.item[0].n_q), b, b.cta_base[b.n], 0, 0, s);
+}
+
+cudaError_t launch_attend_dense(const AttendDense& d, int n_frames, cudaStream_t s) {
+  const TcShape sh = tc_shape(d.a.n_q);
+  return launch_shape(attend_tc_shape(d.a.n_q), d, sh.n_mgroups * d.a.heads * n_frames,
+                      sh.n_mgroups, d.a.n_tiles, s);
 }
 
 }  // namespace pkv

@@ -8,8 +8,10 @@
 // so an error return leaves the cache untouched, and every kernel gets the
 // positions it reads and writes as arguments.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -855,6 +857,70 @@ pkv_status pkv_attend_sampled(pkv_t h, const void* q, int n_q, int sid, int laye
     place_partials(&a, h->d_scratch);
   }
   PKV_CUDA(h, launch_attend(a, h->num_sms, as_stream(cuda_stream)));
+  return PKV_OK;
+}
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (the library
+// does not link the driver library itself).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// Tensor map over a dense [rows][heads][64] bf16 tensor: box of 64 rows x 1
+// head x 64 elements, 128-byte swizzle (the tensor-core operand layout), zero
+// fill past the last row.
+static bool encode_kv_map(CUtensorMap* m, const void* base, int heads, long long rows) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)heads * kHeadDim * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1u, 64u};
+  const cuuint32_t elem[3] = {1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+pkv_status pkv_attend_frames(pkv_t h, const void* q, const void* k, const void* v, int n_frames,
+                             int tokens, void* out, float sm_scale, void* cuda_stream) {
+  if (!h) return fail(h, PKV_ERR_INVALID, "null handle");
+  if (n_frames < 0 || tokens < 1 || tokens > (1 << 20))
+    return fail(h, PKV_ERR_INVALID, "n_frames %d / tokens %d out of range", n_frames, tokens);
+  // the tensor copies address rows with 32-bit coordinates
+  if ((long long)n_frames * tokens > (long long)INT_MAX - 64)
+    return fail(h, PKV_ERR_INVALID, "n_frames x tokens exceeds 2^31 - 65 rows");
+  if (n_frames == 0) return PKV_OK;
+  if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(h, PKV_ERR_INVALID, "q/k/v/out must be 16-byte aligned device pointers");
+  const long long grid = (long long)attend_tc_mgroups(tokens) * h->H * n_frames;
+  if (grid > INT_MAX) return fail(h, PKV_ERR_INVALID, "too many frames for one launch");
+  AttendDense d;
+  std::memset(&d, 0, sizeof(d));
+  const long long rows = (long long)n_frames * tokens;
+  if (!encode_kv_map(&d.k_map, k, h->H, rows) || !encode_kv_map(&d.v_map, v, h->H, rows))
+    return fail(h, PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable or rejected the K/V tensors");
+  AttendArgs& a = d.a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.out = static_cast<uint16_t*>(out);
+  a.n_q = tokens;
+  a.heads = h->H;
+  a.page_size = 64;                 // no pages; keeps the kernel's page arithmetic defined
+  a.n_slots = tokens;
+  a.n_tiles = ceil_div(tokens, 64);
+  const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)h->D);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.num_splits = 1;
+  a.err = h->d_err;
+  PKV_CUDA(h, launch_attend_dense(d, n_frames, as_stream(cuda_stream)));
   return PKV_OK;
 }
 

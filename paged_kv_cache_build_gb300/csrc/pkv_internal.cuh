@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>                   // CUtensorMap (the type only; no driver call here)
 #include <cuda_runtime.h>
 
 #include <utility>
@@ -221,6 +222,18 @@ struct AttendBatch {
   AttendArgs item[kMaxBatch];
 };
 
+// Intra-frame attention (pkv_attend_frames): n_frames independent problems,
+// the tokens of frame f attending to frame f's own tokens. `a` holds the common
+// fields: n_q = tokens per frame (the keys and values are the same tokens),
+// num_splits = 1, no table. K and V are read through 3-D tensor maps over
+// [n_frames * tokens][heads][64] bf16 whose box, 64 tokens x 1 head x 64
+// elements with the 128-byte swizzle, lands as one tensor-core operand tile.
+struct AttendDense {
+  CUtensorMap k_map;
+  CUtensorMap v_map;
+  AttendArgs a;
+};
+
 // ------------------------------------------------------- page sampling
 // vLLM-Omni RFC "Reconstruction Engine", section 5 (KV compression: AVGGT draws
 // a random KV subset per layer): a non-anchor page at table position e is kept
@@ -292,6 +305,8 @@ int attend_tc_mgroups(int n_q);
 int attend_tc_splits_pairs(int pairs, int n_tiles, int num_sms);
 int attend_tc_splits(int n_q, int heads, int n_tiles, int num_sms);
 int attend_tc_tiles(long long n_slots);
+// Intra-frame attention over n_frames frames (grid: M-groups x heads x frames).
+cudaError_t launch_attend_dense(const AttendDense& d, int n_frames, cudaStream_t s);
 cudaError_t launch_synth(uint16_t* dst, int n_frames, int n_tokens, int heads, int head_dim,
                          unsigned long long key_base, int frame0, int token0, float scale,
                          cudaStream_t s);
