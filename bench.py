@@ -51,6 +51,9 @@ def parse():
                    help="run N frames of the stream once, eagerly, and exit (a small case for ncu)")
     p.add_argument("--profile-chunks", type=int, default=0,
                    help="run N chunks of the chunked workload once and exit (a small case for ncu)")
+    p.add_argument("--profile-frame-attn", type=int, default=0,
+                   help="run N intra-frame attention calls on a VGGT chunk's 8 x 1374-token frames "
+                        "and exit (a small case for ncu)")
     p.add_argument("--no-extra", action="store_true", help="skip the extra workload measurements")
     return p.parse_args()
 
@@ -873,9 +876,34 @@ def run_profile_chunked(args):
     print(json.dumps({"profile_chunks": args.profile_chunks}))
 
 
+def run_profile_frame_attn(args):
+    """N intra-frame attention calls (pkv_attend_frames) on one VGGT chunk's 8
+    frames of 1,374 tokens, 16 heads x 64."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_cache_build_gb300 import PagedKVCache, synth_fill
+    from synth import TENSOR_K, TENSOR_Q, TENSOR_V, WORKLOADS
+    w = WORKLOADS["chunked"]
+    x = torch.empty((3, w.chunk_size, w.tokens_per_frame, w.heads, w.head_dim), dtype=torch.bfloat16,
+                    device="cuda")
+    synth_fill(x[0], 0, w.index, 0, 0, 0, TENSOR_Q)
+    synth_fill(x[1], 0, w.index, 0, 0, 0, TENSOR_K)
+    synth_fill(x[2], 0, w.index, 0, 0, 0, TENSOR_V)
+    out = torch.empty_like(x[0])
+    cache = PagedKVCache(4, 16, w.heads, w.head_dim)
+    for _ in range(args.profile_frame_attn):
+        cache.attend_frames(x[0], x[1], x[2], out=out, sm_scale=w.sm_scale)
+    torch.cuda.synchronize()
+    cache.sync()
+    print(json.dumps({"profile_frame_attn": args.profile_frame_attn}))
+
+
 def main():
     args = parse()
-    if args.profile_chunks:
+    if args.profile_frame_attn:
+        run_profile_frame_attn(args)
+    elif args.profile_chunks:
         run_profile_chunked(args)
     elif args.profile_frames:
         run_profile(args)

@@ -374,18 +374,38 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
                  "r"(TmemCols<MT>::kAlloc));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
+  // barriers initialised and the zeroed ring visible to the copy engine: from
+  // here the producer may fill the ring
+  fence_proxy_async();
+  __syncthreads();
   // everything above is private to the CTA; inputs are read only after the
   // previous kernel on the stream has completed
   pdl_wait();
   pdl_trigger();
-  {
-    for (int i = threadIdx.x; i < MT * 128 * 8; i += blockDim.x) {
-      const int m = i / (128 * 8), r = (i >> 3) & 127, c = i & 7;
-      const int row = row0 + m * 128 + r;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (row < a.n_q)
-        val = __ldg(reinterpret_cast<const uint4*>(qg + ((long long)row * H + h) * kHeadDim + c * 8));
-      *reinterpret_cast<uint4*>(&sm.q[m][r * 128 + (swizzle_chunk(r, c) << 4)]) = val;
+  if (warp != kProducerWarp) {
+    // Q tiles: every load issued before the first store; the producer warp
+    // meanwhile starts on the KV ring
+    constexpr int kThreads = tc_threads<MT, EXTRA>() - 32;
+    constexpr int kQ = MT * 128 * 8;               // 16-byte chunks
+    constexpr int kQPer = (kQ + kThreads - 1) / kThreads;
+    const int qt = warp < kProducerWarp ? (int)threadIdx.x : (int)threadIdx.x - 32;
+    uint4 val[kQPer];
+#pragma unroll
+    for (int u = 0; u < kQPer; ++u) {
+      const int i = qt + u * kThreads;
+      const int row = row0 + (i >> 3);             // M-tile m rows follow m * 128
+      val[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < kQ && row < a.n_q)
+        val[u] = __ldg(reinterpret_cast<const uint4*>(qg + ((long long)row * H + h) * kHeadDim +
+                                                      (i & 7) * 8));
+    }
+#pragma unroll
+    for (int u = 0; u < kQPer; ++u) {
+      const int i = qt + u * kThreads;
+      if (i < kQ) {
+        const int m = i / (128 * 8), r = (i >> 3) & 127, c = i & 7;
+        *reinterpret_cast<uint4*>(&sm.q[m][r * 128 + (swizzle_chunk(r, c) << 4)]) = val[u];
+      }
     }
     fence_proxy_async();
   }
@@ -411,9 +431,13 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   int e_batch = e_first & ~31, e_page = 0, e_len = 0;
   if (warp == kProducerWarp && e_batch + lane < a.n_entries)
     table_entry(a.tbl, entry_of(e_batch + lane), e_page, e_len);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  // Q and the TMEM address published to every role but the producer, which
+  // needs neither (named barrier 1: all warps but the producer)
+  if (warp != kProducerWarp) {
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;\n" ::"r"(tc_threads<MT, EXTRA>() - 32) : "memory");
+    tc_fence_after();
+  }
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
 
