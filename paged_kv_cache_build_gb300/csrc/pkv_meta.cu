@@ -50,6 +50,24 @@ __global__ void __launch_bounds__(512) frame_append_kernel(const FrameAppendArgs
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.y;
+  const AppendItem& it = a.item[b];
+  const int H = a.pool.heads;
+  const int hh = threadIdx.x >> 3, c = threadIdx.x & 7;
+  const bool mover = hh < 2 * H;               // blocks have at least one full warp
+  const int kv = hh >= H ? 1 : 0;
+  const int h = hh - kv * H;
+  const int T = a.n_patch + a.n_special;
+  const int t0 = blockIdx.x * TPB;
+  // The block's K/V rows are loaded first: they do not depend on the page pop
+  // below, whose dependent loads then overlap them.
+  uint4 val[TPB];
+  if (mover) {
+    const uint16_t* src = (kv ? it.v : it.k) + (long long)h * kHeadDim + c * 8;
+#pragma unroll
+    for (int i = 0; i < TPB; ++i)
+      if (t0 + i < T)
+        val[i] = __ldg(reinterpret_cast<const uint4*>(src + (long long)(t0 + i) * H * kHeadDim));
+  }
   __shared__ int s_patch, s_sp;
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
@@ -62,7 +80,6 @@ __global__ void __launch_bounds__(512) frame_append_kernel(const FrameAppendArgs
     }
     const int off = __shfl_sync(0xffffffffu, incl - need, b);
     if (lane == 0) {
-      const AppendItem& it = a.item[b];
       int patch, sp;
       if (a.is_meta) {
         patch = a.free_stack[a.top - 1 - off];
@@ -85,22 +102,7 @@ __global__ void __launch_bounds__(512) frame_append_kernel(const FrameAppendArgs
   }
   __syncthreads();
   const int patch = s_patch, sp = s_sp;
-  if (patch < 0) return;
-
-  const AppendItem& it = a.item[b];
-  const int H = a.pool.heads;
-  const int hh = threadIdx.x >> 3, c = threadIdx.x & 7;
-  if (hh >= 2 * H) return;                   // blocks have at least one full warp
-  const int kv = hh >= H ? 1 : 0;
-  const int h = hh - kv * H;
-  const int T = a.n_patch + a.n_special;
-  const int t0 = blockIdx.x * TPB;
-  const uint16_t* src = (kv ? it.v : it.k) + (long long)h * kHeadDim + c * 8;
-  uint4 val[TPB];
-#pragma unroll
-  for (int i = 0; i < TPB; ++i)
-    if (t0 + i < T)
-      val[i] = __ldg(reinterpret_cast<const uint4*>(src + (long long)(t0 + i) * H * kHeadDim));
+  if (patch < 0 || !mover) return;
 #pragma unroll
   for (int i = 0; i < TPB; ++i) {
     const int t = t0 + i;
