@@ -33,7 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "frame-steps/s and attn TFLOP/s (bf16 paged stream attn) vs GB300 roofline"
-HOST_COVER_CYCLES = 100_000   # ~50 us of GPU busy-wait ahead of a per-call timing
+HOST_COVER_CYCLES = 400_000   # ~200 us of GPU busy-wait ahead of a per-call timing, longer than the host needs to queue the call
 UNIT = "frame-steps/s"
 WORKLOAD_NAME = "lingbot-1layer-512f-256p+6s-16x64-S8-W64"
 
@@ -672,19 +672,18 @@ def run_ours(args):
     attn_tflops = att_flops / (att_ms * 1e-3) / 1e12
     steady_tflops = steady_flops / (steady_ms * 1e-3) / 1e12
 
-    # ---- end to end through the C ABI with host buffers (pinned), eager calls.
-    # Each step copies every frame's q, k, v from pinned host memory and every
-    # output back, in chunks of 64 frames on a copy stream that runs ahead of the
-    # compute stream (one H2D and one D2H per chunk, ordered with events), while
-    # the compute stream makes the per-frame C-ABI calls.
-    FB = T * H * D                                   # elements of one [T][H][D] tensor
-    hin = torch.empty((F, 3, T, H, D), dtype=torch.bfloat16, pin_memory=True)
-    hin[:, 0].copy_(q)
-    hin[:, 1].copy_(k)
-    hin[:, 2].copy_(v)
+    # ---- end to end through the C ABI with host buffers (pinned). Each step
+    # copies every frame's q, k, v from pinned host memory and every output back,
+    # in chunks of 64 frames on a copy stream that runs ahead of the compute
+    # stream (three H2D copies and one D2H per chunk, ordered with events), while
+    # the compute stream runs each chunk's frames with one pkv_stream_frames call
+    # (append, attend, evict per frame, driven from native code).
+    hq, hk, hv = (torch.empty((F, T, H, D), dtype=torch.bfloat16, pin_memory=True) for _ in range(3))
+    hq.copy_(q)
+    hk.copy_(k)
+    hv.copy_(v)
     hout = torch.empty((F, T, H, D), dtype=torch.bfloat16, pin_memory=True)
-    din = torch.empty((F, 3, T, H, D), dtype=torch.bfloat16, device=device)
-    dout = torch.empty((F, T, H, D), dtype=torch.bfloat16, device=device)
+    dq, dk, dv, dout = (torch.empty((F, T, H, D), dtype=torch.bfloat16, device=device) for _ in range(4))
     chunk = 64
     copy_stream = torch.cuda.Stream(device=device)
     comp_stream = torch.cuda.current_stream(device)
@@ -696,26 +695,26 @@ def run_ours(args):
     t_wall = time.perf_counter()
     f0.record()
     sp = ctypes.c_void_p(comp_stream.cuda_stream)
-    esz = 2                                          # bytes per bf16
+    fbytes = T * H * D * 2                           # bytes of one [T][H][D] bf16 tensor
     for _ in range(n_e2e):
         check(lib.pkv_stream_reset(h, sid, sp))
-        copy_stream.wait_stream(comp_stream)         # the previous step is done with din/dout
+        copy_stream.wait_stream(comp_stream)         # the previous step is done with dq/dk/dv/dout
         arrived, computed = [], []
         with torch.cuda.stream(copy_stream):
             for c0 in range(0, F, chunk):
-                din[c0:c0 + chunk].copy_(hin[c0:c0 + chunk], non_blocking=True)
+                for dst, src in ((dq, hq), (dk, hk), (dv, hv)):
+                    dst[c0:c0 + chunk].copy_(src[c0:c0 + chunk], non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(copy_stream)
                 arrived.append(ev)
         for ci, c0 in enumerate(range(0, F, chunk)):
             comp_stream.wait_event(arrived[ci])
-            for t in range(c0, min(F, c0 + chunk)):
-                base = din.data_ptr() + t * 3 * FB * esz
-                check(lib.pkv_append_frame(h, sid, 0, ctypes.c_void_p(base + FB * esz),
-                                           ctypes.c_void_p(base + 2 * FB * esz), T, sp))
-                check(lib.pkv_attend(h, ctypes.c_void_p(base), T, sid, 0,
-                                     ctypes.c_void_p(dout.data_ptr() + t * FB * esz), scale, sp))
-                check(lib.pkv_evict_window(h, sid, sp))
+            n = min(F, c0 + chunk) - c0
+            off = c0 * fbytes
+            check(lib.pkv_stream_frames(h, sid, 0, ctypes.c_void_p(dq.data_ptr() + off),
+                                        ctypes.c_void_p(dk.data_ptr() + off),
+                                        ctypes.c_void_p(dv.data_ptr() + off), n, T, None,
+                                        ctypes.c_void_p(dout.data_ptr() + off), scale, sp))
             ev = torch.cuda.Event()
             ev.record(comp_stream)
             computed.append(ev)

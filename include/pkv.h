@@ -167,6 +167,31 @@ pkv_status pkv_rollback_last_frame(pkv_t h, int stream_id, void* cuda_stream);
  * Errors: OOM if a reset cannot pop its special page. */
 pkv_status pkv_evict_window(pkv_t h, int stream_id, void* cuda_stream);
 
+/* A run of n_frames frames of one frame-mode stream, driven from native code
+ * (sections 2-3 of "LingBot-Map Paged KV Cache": each new frame is appended,
+ * attends over the visible pages, then is committed with pkv_evict_window when it
+ * is a keyframe or undone with pkv_rollback_last_frame when it is not). For
+ * every frame t in order it makes exactly these calls on cuda_stream:
+ *   pkv_append_frame(h, stream_id, layer, k[t], v[t], tokens)
+ *   pkv_attend(h, q[t], tokens, stream_id, layer, out[t], sm_scale)
+ *   keyframe == NULL || keyframe[t] ? pkv_evict_window : pkv_rollback_last_frame
+ * so results and state equal those of the separate calls; only the host work per
+ * frame shrinks (no caller round trip between the calls).
+ * q, k, v, out: device bf16 [n_frames][tokens][heads][64], contiguous, 16-byte
+ * aligned, owned by the caller; keyframe: HOST array of n_frames bytes, or NULL
+ * (every frame is a keyframe). tokens must be the stream's n_patch + n_special.
+ * With several layers, a frame's evict or rollback follows its append and attend
+ * of `layer` alone, so this drives one-layer streams (or callers that run one
+ * layer per stream). n_frames = 0 is a no-op.
+ * Errors: INVALID (null or unaligned pointer, tokens, layer, n_frames < 0), STATE
+ * (a chunked-mode stream, or a frame of this stream is pending); else the first
+ * failing call's status, with the frame's index in pkv_last_error. Frames before
+ * the failing one stay applied (each call is all-or-nothing, the run is not). */
+pkv_status pkv_stream_frames(pkv_t h, int stream_id, int layer, const void* q, const void* k,
+                             const void* v, int n_frames, int tokens,
+                             const unsigned char* keyframe, void* out, float sm_scale,
+                             void* cuda_stream);
+
 /* Write the visible page table (section 2, build_visible_page_table): page ids in
  * the order scale -> window (oldest first) -> special (allocation order); chunked
  * mode: chunks oldest first, pages in order.

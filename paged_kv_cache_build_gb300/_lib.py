@@ -46,6 +46,8 @@ SIGNATURES = {
                                    c_void_p]),
     "pkv_attend_frames": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_void_p,
                                   c_float, c_void_p]),
+    "pkv_stream_frames": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p, c_int,
+                                  c_int, c_void_p, c_void_p, c_float, c_void_p]),
     "pkv_sync": (c_int, [c_void_p, c_void_p]),
     "pkv_visible_count": (c_int, [c_void_p, c_int, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]),
     "pkv_free_pages": (c_int, [c_void_p, ctypes.POINTER(c_int)]),

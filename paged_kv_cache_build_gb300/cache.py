@@ -171,6 +171,29 @@ class PagedKVCache:
                                                _stream_ptr(stream)))
         return out
 
+    def stream_frames(self, sid, q, k, v, keyframe=None, layer=0, out=None, sm_scale=0.0,
+                      stream=None):
+        """pkv_stream_frames: for each frame t, append k[t]/v[t], attend q[t] into
+        out[t], then evict (keyframe[t] true or keyframe None) or roll back.
+        q, k, v: [n_frames][tokens][heads][64] contiguous bf16 CUDA tensors."""
+        if q.shape != k.shape or q.shape != v.shape or q.dim() != 4:
+            raise ValueError("q, k and v must share the shape [n_frames][tokens][heads][64]")
+        n_frames, tokens = q.shape[0], q.shape[1]
+        if out is None:
+            out = torch.empty_like(q)
+        flags = None
+        if keyframe is not None:
+            if len(keyframe) != n_frames:
+                raise ValueError("one keyframe flag per frame")
+            flags = (ctypes.c_ubyte * n_frames)(*[1 if f else 0 for f in keyframe])
+        self._check(self.lib.pkv_stream_frames(self.h, sid, layer, _bf16_ptr(q, "q"),
+                                               _bf16_ptr(k, "k"), _bf16_ptr(v, "v"), n_frames,
+                                               tokens,
+                                               ctypes.cast(flags, ctypes.c_void_p) if flags else None,
+                                               _bf16_ptr(out, "out"),
+                                               float(sm_scale), _stream_ptr(stream)))
+        return out
+
     def attend_noalloc(self, q, sid, layer=0, out=None, sm_scale=0.0, stream=None):
         """pkv_attend_noalloc: attention whose scratch is a fixed device array."""
         if out is None:

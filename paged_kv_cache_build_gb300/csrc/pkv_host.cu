@@ -805,6 +805,42 @@ pkv_status pkv_attend(pkv_t h, const void* q, int n_q, int sid, int layer, void*
   return attend_common(h, st, q, n_q, layer, out, sm_scale, as_stream(cuda_stream));
 }
 
+pkv_status pkv_stream_frames(pkv_t h, int sid, int layer, const void* q, const void* k,
+                             const void* v, int n_frames, int tokens,
+                             const unsigned char* keyframe, void* out, float sm_scale,
+                             void* cuda_stream) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  if (st->cfg.mode != PKV_MODE_FRAME)
+    return fail(h, PKV_ERR_STATE, "pkv_stream_frames needs a frame-mode stream");
+  if (st->pending) return fail(h, PKV_ERR_STATE, "a frame of stream %d is pending", sid);
+  if (n_frames < 0) return fail(h, PKV_ERR_INVALID, "n_frames %d < 0", n_frames);
+  if (layer < 0 || layer >= h->L) return fail(h, PKV_ERR_INVALID, "layer %d out of range", layer);
+  if (tokens != st->cfg.n_patch + st->cfg.n_special)
+    return fail(h, PKV_ERR_INVALID, "tokens %d != n_patch + n_special", tokens);
+  if (n_frames == 0) return PKV_OK;
+  if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(h, PKV_ERR_INVALID, "q/k/v/out must be 16-byte aligned device pointers");
+  const size_t fb = (size_t)tokens * h->H * kHeadDim * sizeof(uint16_t);   // bytes per frame
+  const char* qb = static_cast<const char*>(q);
+  const char* kb = static_cast<const char*>(k);
+  const char* vb = static_cast<const char*>(v);
+  char* ob = static_cast<char*>(out);
+  for (int t = 0; t < n_frames; ++t) {
+    const size_t o = fb * (size_t)t;
+    pkv_status r = pkv_append_frame(h, sid, layer, kb + o, vb + o, tokens, cuda_stream);
+    if (r == PKV_OK) r = pkv_attend(h, qb + o, tokens, sid, layer, ob + o, sm_scale, cuda_stream);
+    if (r == PKV_OK)
+      r = (keyframe == nullptr || keyframe[t]) ? pkv_evict_window(h, sid, cuda_stream)
+                                               : pkv_rollback_last_frame(h, sid, cuda_stream);
+    if (r != PKV_OK) {
+      h->last_error = "frame " + std::to_string(t) + ": " + h->last_error;
+      return r;
+    }
+  }
+  return PKV_OK;
+}
+
 pkv_status pkv_attend_chunked(pkv_t h, const void* q, int n_q, int sid, int layer, void* out,
                               float sm_scale, void* cuda_stream) {
   Stream* st = nullptr;
