@@ -55,3 +55,18 @@ def test_host_side_errors_without_gpu(lib):
     assert L.pkv_create(0, 256, 16, 64, ctypes.byref(h)) == 1        # empty pool
     assert L.pkv_destroy(None) == 0
     assert L.pkv_synth_fill(None, 1, 1, 1, 64, 0, 0, 0, 0, 0, 0, 0, 1.0, None) == 1
+
+
+def test_null_handle_is_rejected_without_gpu(lib):
+    """Every entry point that takes a handle rejects a null one (PKV_ERR_INVALID)
+    before any CUDA call."""
+    from paged_kv_cache_build_gb300._lib import load
+    L = load()
+    f = ctypes.c_float(0.125)
+    assert L.pkv_attend_frames(None, None, None, None, 1, 16, None, f, None) == 1
+    assert b"null handle" in L.pkv_last_error(None)
+    assert L.pkv_stream_frames(None, 0, 0, None, None, None, 1, 16, None, None, f, None) == 1
+    assert L.pkv_attend(None, None, 1, 0, 0, None, f, None) == 1
+    assert L.pkv_attend_sampled(None, None, 1, 0, 0, None, f, 1, 1, None) == 1
+    assert L.pkv_evict_window(None, 0, None) == 1
+    assert L.pkv_rollback_last_frame(None, 0, None) == 1
