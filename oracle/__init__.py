@@ -22,7 +22,8 @@ Sources (page title, section):
     current chunk, KV append, evict the oldest chunk); section 2.2 and 3.3
     (frame attention, each frame's tokens over that frame's own tokens,
     alternating with the global attention); section 5 (KV compression: the
-    per-layer random page subset of sampling.py).
+    per-layer random page subset of sampling.py, and the page skipping by
+    estimated attention mass of blocksparse.py).
 
 Parity of every function here is pinned in tests/test_oracle_*.py against a
 brute-force flat model, closed forms, a library softmax-attention routine and
