@@ -555,6 +555,50 @@ def extra_sampled(frames=150, reps=20):
             "speedup_quarter": round(res[65536] / res[16384], 2)}
 
 
+def extra_blocksparse(frames=150, reps=20):
+    """The same steady-state frame attending to the scale pages plus the `keep`
+    visible pages of highest estimated attention mass (pkv_attend_blocksparse: the
+    estimate, the selection and the attention all on the device): us per call
+    keeping every page, a quarter and an eighth of the non-anchor pages."""
+    import torch
+    from paged_kv_cache_build_gb300 import PagedKVCache, frame_stream_cfg, synth_fill
+    from synth import TENSOR_K, TENSOR_Q, TENSOR_V, WORKLOADS
+    w = WORKLOADS["lingbot"]
+    T, H, D = w.frame_tokens, w.heads, w.head_dim
+    cache = PagedKVCache(w.pool_pages, w.page_size, H, D)
+    sid = cache.open_stream(frame_stream_cfg(w.num_scale, w.window, w.n_patch, w.n_special))
+    kv = torch.empty((2, 8, T, H, D), dtype=torch.bfloat16, device="cuda")
+    synth_fill(kv[0], 0, w.index, 0, 0, 0, TENSOR_K)
+    synth_fill(kv[1], 0, w.index, 0, 0, 0, TENSOR_V)
+    for t in range(frames):
+        cache.append_frame(sid, kv[0, t % 8], kv[1, t % 8])
+        if t < frames - 1:
+            cache.evict_window(sid)
+    q = torch.empty((T, H, D), dtype=torch.bfloat16, device="cuda")
+    synth_fill(q, 0, w.index, 0, 0, 0, TENSOR_Q, 0, w.q_scale)
+    out = torch.empty_like(q)
+    n_other = cache.visible_count(sid)[0] - w.num_scale
+    res = {}
+    for name, keep in (("all", n_other), ("quarter", n_other // 4), ("eighth", n_other // 8)):
+        times = []
+        for r in range(reps + 3):
+            e0, e1 = _events()
+            torch.cuda._sleep(HOST_COVER_CYCLES)
+            e0.record()
+            cache.attend_blocksparse(q, sid, 0, keep=keep, out=out, sm_scale=w.sm_scale)
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 3:
+                times.append(e0.elapsed_time(e1))
+        res[name] = statistics.median(times) * 1e3
+    cache.sync()
+    cache.close()
+    return {"workload": "lingbot frame %d, one layer, %d non-anchor pages" % (frames - 1, n_other),
+            "us_keep_all": round(res["all"], 2), "us_keep_quarter": round(res["quarter"], 2),
+            "us_keep_eighth": round(res["eighth"], 2),
+            "speedup_quarter": round(res["all"] / res["quarter"], 2)}
+
+
 # ------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -762,7 +806,8 @@ def run_ours(args):
     if not args.no_extra:
         line["extra"] = {"chunked": extra_chunked(), "long24": extra_long24(), "append": extra_append(),
                          "multistream": extra_multistream(), "sampled": extra_sampled(),
-                         "frames": extra_frames(), "model24": extra_long24(frame_attn=True)}
+                         "frames": extra_frames(), "model24": extra_long24(frame_attn=True),
+                         "blocksparse": extra_blocksparse()}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)

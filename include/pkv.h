@@ -254,6 +254,34 @@ pkv_status pkv_attend_sampled(pkv_t h, const void* q, int n_q, int stream_id, in
 pkv_status pkv_attend_frames(pkv_t h, const void* q, const void* k, const void* v, int n_frames,
                              int tokens, void* out, float sm_scale, void* cuda_stream);
 
+/* Frame-mode attention over the visible pages with the highest estimated attention
+ * mass. vLLM-Omni RFC "Reconstruction Engine", section 5 (KV compression):
+ * Sparse-VGGT observes that global attention mass concentrates on a few blocks and
+ * skips the low-weight ones; FastVGGT keeps the initial frames as anchors. Read at
+ * page granularity on the visible table of "LingBot-Map Paged KV Cache", section 2:
+ * the scale pages are always kept; every other visible page e gets the estimate
+ *   score(e) = sum over h, d of qm[h][d] * km_e[h][d]
+ * where qm is the mean over the call's n_q query rows and km_e the mean over page
+ * e's valid slots of the layer's keys; the `keep` pages with the highest score are
+ * kept (ties to the earlier table position; a NaN score ranks lowest). The score
+ * decides which pages are kept, so it is computed in IEEE fp32 in a fixed order:
+ * each mean a running sum in row (slot) order divided once, then one running sum
+ * over h and d in that order of the rounded products (no fused multiply-add).
+ * The attention is pkv_attend's over the kept pages' valid slots, in table order.
+ * keep >= 0 (at least the number of non-anchor pages keeps them all). The
+ * estimate, the selection and the attention all run on the device (no host
+ * round trip); the first call allocates a small device buffer.
+ * Errors: as pkv_attend; STATE for a chunked-mode stream; INVALID for keep < 0 or
+ * more than 1024 visible pages. */
+pkv_status pkv_attend_blocksparse(pkv_t h, const void* q, int n_q, int stream_id, int layer,
+                                  void* out, float sm_scale, int keep, void* cuda_stream);
+
+/* The table positions kept by the last pkv_attend_blocksparse call on this handle,
+ * in table order (a readback for tests and diagnostics). kept_out: HOST int array
+ * of `capacity` entries; *n_out receives the count. Synchronizes the device.
+ * Errors: INVALID (null pointer, capacity too small), STATE (no such call yet). */
+pkv_status pkv_blocksparse_kept(pkv_t h, int* kept_out, int capacity, int* n_out);
+
 /* Several streams' attention in one launch (the multi-stream pool of LingBot-Map
  * section 4; batching in the manner of the vLLM-Omni RFC's scheduler, section
  * 2.3). Equivalent to n calls of pkv_attend (frame-mode streams) or

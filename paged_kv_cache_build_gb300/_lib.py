@@ -44,6 +44,9 @@ SIGNATURES = {
                                    c_int, c_int, c_void_p, c_float, c_void_p]),
     "pkv_attend_noalloc": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_float,
                                    c_void_p]),
+    "pkv_attend_blocksparse": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_float,
+                                       c_int, c_void_p]),
+    "pkv_blocksparse_kept": (c_int, [c_void_p, ctypes.POINTER(c_int), c_int, ctypes.POINTER(c_int)]),
     "pkv_attend_frames": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_void_p,
                                   c_float, c_void_p]),
     "pkv_stream_frames": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p, c_int,

@@ -133,6 +133,23 @@ class PagedKVCache:
                                                 int(keep), _stream_ptr(stream)))
         return out
 
+    def attend_blocksparse(self, q, sid, layer=0, keep=0, out=None, sm_scale=0.0, stream=None):
+        """pkv_attend_blocksparse: attention over the scale pages and the `keep`
+        other visible pages with the highest estimated attention mass."""
+        if out is None:
+            out = torch.empty_like(q)
+        self._check(self.lib.pkv_attend_blocksparse(self.h, _bf16_ptr(q, "q"), q.shape[0], sid,
+                                                    layer, _bf16_ptr(out, "out"), float(sm_scale),
+                                                    int(keep), _stream_ptr(stream)))
+        return out
+
+    def blocksparse_kept(self):
+        """Table positions kept by the last attend_blocksparse call, in order."""
+        buf = (ctypes.c_int * 1024)()
+        n = ctypes.c_int(0)
+        self._check(self.lib.pkv_blocksparse_kept(self.h, buf, 1024, ctypes.byref(n)))
+        return list(buf[:n.value])
+
     def attend_batched(self, qs, sids, layer=0, sm_scale=0.0, stream=None):
         """pkv_attend_batched: the streams' attention in one launch. qs: one
         [n_q][heads][64] bf16 tensor per stream (packed into one buffer here);

@@ -414,14 +414,19 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   // A sampled call's kept table positions, in order (producer warp, a ballot
   // per 32 positions); the producer then indexes the kept pages only.
   if (warp == kProducerWarp && a.sampled) {
-    int count = 0;
-    for (int e0 = 0; e0 < a.n_entries_all; e0 += 32) {
-      const int e = e0 + lane;
-      const bool keep = e < a.n_entries_all &&
-                        (e < a.sample_anchor || page_sample_kept(a.sample_key, e, a.sample_keep));
-      const unsigned ball = __ballot_sync(0xffffffffu, keep);
-      if (keep) sm.kept[count + __popc(ball & ((1u << lane) - 1u))] = (uint16_t)e;
-      count += __popc(ball);
+    if (a.kept_dev) {
+      // a list made on the device (page skipping by estimated mass)
+      for (int i = lane; i < a.n_entries; i += 32) sm.kept[i] = __ldcg(a.kept_dev + i);
+    } else {
+      int count = 0;
+      for (int e0 = 0; e0 < a.n_entries_all; e0 += 32) {
+        const int e = e0 + lane;
+        const bool keep = e < a.n_entries_all &&
+                          (e < a.sample_anchor || page_sample_kept(a.sample_key, e, a.sample_keep));
+        const unsigned ball = __ballot_sync(0xffffffffu, keep);
+        if (keep) sm.kept[count + __popc(ball & ((1u << lane) - 1u))] = (uint16_t)e;
+        count += __popc(ball);
+      }
     }
     __syncwarp();
   }

@@ -67,6 +67,8 @@ struct pkv_ctx {
   std::vector<Stream> streams;
   float* d_scratch = nullptr;
   size_t scratch_bytes = 0;
+  void* d_select = nullptr;      // page skipping: query means, page estimates, kept list
+  int select_kept = 0;           // entries in that kept list (the last call's)
   int num_sms = 0;
   std::string last_error;
 };
@@ -280,6 +282,7 @@ pkv_status pkv_destroy(pkv_t h) {
   if (h->d_free) cudaFree(h->d_free);
   if (h->d_err) cudaFree(h->d_err);
   if (h->d_scratch) cudaFree(h->d_scratch);
+  if (h->d_select) cudaFree(h->d_select);
   delete h;
   return PKV_OK;
 }
@@ -893,6 +896,79 @@ pkv_status pkv_attend_sampled(pkv_t h, const void* q, int n_q, int sid, int laye
     place_partials(&a, h->d_scratch);
   }
   PKV_CUDA(h, launch_attend(a, h->num_sms, as_stream(cuda_stream)));
+  return PKV_OK;
+}
+
+pkv_status pkv_attend_blocksparse(pkv_t h, const void* q, int n_q, int sid, int layer, void* out,
+                                  float sm_scale, int keep, void* cuda_stream) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  if (st->cfg.mode != PKV_MODE_FRAME)
+    return fail(h, PKV_ERR_STATE, "pkv_attend_blocksparse needs a frame-mode stream");
+  if (keep < 0) return fail(h, PKV_ERR_INVALID, "keep %d < 0", keep);
+  AttendArgs a;
+  if (pkv_status r = attend_args(h, st, q, n_q, layer, out, sm_scale, &a)) return r;
+  const int np = a.n_entries;
+  if (np > kMaxSampledEntries)
+    return fail(h, PKV_ERR_INVALID, "%d visible pages; this call takes at most %d", np,
+                kMaxSampledEntries);
+  if (!h->d_select) {
+    const size_t bytes = sizeof(float) * (kMaxHeads * kHeadDim + kMaxSampledEntries) +
+                         sizeof(uint16_t) * kMaxSampledEntries;
+    PKV_CUDA(h, cudaMalloc(&h->d_select, bytes));
+  }
+  float* qm = static_cast<float*>(h->d_select);
+  float* scores = qm + kMaxHeads * kHeadDim;
+  uint16_t* kept = reinterpret_cast<uint16_t*>(scores + kMaxSampledEntries);
+  const int n_anchor = a.tbl.n_scale;
+  const int n_kept = n_anchor + std::min(keep, np - n_anchor);
+  PageScoreArgs g;
+  std::memset(&g, 0, sizeof(g));
+  g.q = static_cast<const uint16_t*>(q);
+  g.n_q = n_q;
+  g.heads = h->H;
+  g.pool = pool_view(h, layer);
+  g.tbl = a.tbl;
+  g.n_entries = np;
+  g.n_anchor = n_anchor;
+  g.keep = keep;
+  g.qm = qm;
+  g.scores = scores;
+  g.kept = kept;
+  g.err = h->d_err;
+  cudaStream_t s = as_stream(cuda_stream);
+  PKV_CUDA(h, launch_page_select(g, s));
+  h->select_kept = n_kept;
+  // which pages are kept is known on the device only: unless every page is kept
+  // (then the exact slot count of pkv_attend), the grid covers n_kept full pages,
+  // and the slots past each kept page's length are masked
+  a.sampled = 1;
+  a.kept_dev = kept;
+  a.n_entries_all = np;
+  if (n_kept < np) a.n_slots = (long long)n_kept * h->Ps;
+  a.n_entries = n_kept;
+  a.n_tiles = ceil_div(a.n_slots, 64);
+  a.num_splits = attend_num_splits(n_q, h->H, a.n_slots, h->num_sms);
+  if (a.num_splits > 1) {
+    if (pkv_status r = ensure_scratch(h, partial_bytes(a))) return r;
+    place_partials(&a, h->d_scratch);
+  }
+  PKV_CUDA(h, launch_attend(a, h->num_sms, s));
+  return PKV_OK;
+}
+
+pkv_status pkv_blocksparse_kept(pkv_t h, int* kept_out, int capacity, int* n_out) {
+  if (!h || !kept_out || !n_out) return fail(h, PKV_ERR_INVALID, "null argument");
+  if (!h->d_select) return fail(h, PKV_ERR_STATE, "no pkv_attend_blocksparse call yet");
+  if (capacity < h->select_kept)
+    return fail(h, PKV_ERR_INVALID, "capacity %d < %d entries", capacity, h->select_kept);
+  std::vector<uint16_t> tmp(h->select_kept);
+  const uint16_t* kept = reinterpret_cast<const uint16_t*>(
+      static_cast<const float*>(h->d_select) + kMaxHeads * kHeadDim + kMaxSampledEntries);
+  PKV_CUDA(h, cudaDeviceSynchronize());
+  PKV_CUDA(h, cudaMemcpy(tmp.data(), kept, sizeof(uint16_t) * tmp.size(), cudaMemcpyDeviceToHost));
+  for (size_t i = 0; i < tmp.size(); ++i) kept_out[i] = tmp[i];
+  *n_out = h->select_kept;
   return PKV_OK;
 }
 

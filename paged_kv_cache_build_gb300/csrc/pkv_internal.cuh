@@ -200,6 +200,9 @@ struct AttendArgs {
   int sample_anchor;
   int n_entries_all;
   unsigned long long sample_key;
+  // A kept list computed on the device (pkv_attend_blocksparse): the first
+  // n_entries table positions, in order; when set, it replaces the rule above.
+  const uint16_t* kept_dev;
   int n_entries;
   int n_tiles;                      // 64-slot tiles covering the table's slots
   long long n_slots;                // flat slots up to the last valid one
@@ -249,6 +252,29 @@ __host__ __device__ inline bool page_sample_kept(unsigned long long key, int e, 
   z ^= z >> 31;
   return (int)(z & 0xFFFFull) < keep;
 }
+
+// ------------------------------------------- page skipping by estimated mass
+// vLLM-Omni RFC "Reconstruction Engine", section 5 (Sparse-VGGT skips the
+// low-weight blocks; FastVGGT keeps anchors): each visible page of a frame-mode
+// table gets an fp32 estimate (mean query . mean key, summed over heads, in a
+// fixed order); the n_anchor scale pages and the `keep` best others are listed,
+// in table order, in kept[].
+constexpr int kMaxHeads = 32;
+struct PageScoreArgs {
+  const uint16_t* q;                // [n_q][heads][64]
+  int n_q;
+  int heads;
+  PoolView pool;                    // the attended layer's page set
+  TableArgs tbl;
+  int n_entries;                    // visible pages (<= kMaxSampledEntries)
+  int n_anchor;
+  int keep;
+  float* qm;                        // [heads][64] scratch
+  float* scores;                    // [n_entries] scratch
+  uint16_t* kept;                   // [n_anchor + keep] out
+  int* err;
+};
+cudaError_t launch_page_select(const PageScoreArgs& a, cudaStream_t s);
 
 // Kernel launches made by this library in this process (every launcher counts).
 // ---------------------------------------------------- dependent launches
