@@ -914,12 +914,14 @@ pkv_status pkv_attend_blocksparse(pkv_t h, const void* q, int n_q, int sid, int 
                 kMaxSampledEntries);
   if (!h->d_select) {
     const size_t bytes = sizeof(float) * (kMaxHeads * kHeadDim + kMaxSampledEntries) +
-                         sizeof(uint16_t) * kMaxSampledEntries;
+                         sizeof(uint16_t) * kMaxSampledEntries +
+                         sizeof(float) * (size_t)kMaxSampledEntries * kMaxHeads * kHeadDim;
     PKV_CUDA(h, cudaMalloc(&h->d_select, bytes));
   }
   float* qm = static_cast<float*>(h->d_select);
   float* scores = qm + kMaxHeads * kHeadDim;
   uint16_t* kept = reinterpret_cast<uint16_t*>(scores + kMaxSampledEntries);
+  float* prod = reinterpret_cast<float*>(kept + kMaxSampledEntries);   // 16-byte aligned
   const int n_anchor = a.tbl.n_scale;
   const int n_kept = n_anchor + std::min(keep, np - n_anchor);
   PageScoreArgs g;
@@ -934,6 +936,7 @@ pkv_status pkv_attend_blocksparse(pkv_t h, const void* q, int n_q, int sid, int 
   g.keep = keep;
   g.qm = qm;
   g.scores = scores;
+  g.prod = prod;
   g.kept = kept;
   g.err = h->d_err;
   cudaStream_t s = as_stream(cuda_stream);

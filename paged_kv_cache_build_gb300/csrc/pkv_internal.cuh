@@ -260,6 +260,7 @@ __host__ __device__ inline bool page_sample_kept(unsigned long long key, int e, 
 // fixed order); the n_anchor scale pages and the `keep` best others are listed,
 // in table order, in kept[].
 constexpr int kMaxHeads = 32;
+constexpr int kMaxPageSize = 256;
 struct PageScoreArgs {
   const uint16_t* q;                // [n_q][heads][64]
   int n_q;
@@ -271,6 +272,7 @@ struct PageScoreArgs {
   int keep;
   float* qm;                        // [heads][64] scratch
   float* scores;                    // [n_entries] scratch
+  float* prod;                      // [n_entries][heads][64] scratch: qm * km per page
   uint16_t* kept;                   // [n_anchor + keep] out
   int* err;
 };

@@ -27,47 +27,87 @@ __device__ __forceinline__ float bf16_at(const uint16_t* p) {
   return __uint_as_float((uint32_t)__ldg(p) << 16);
 }
 
-// qm[h][d]: block h, thread d
-__global__ void __launch_bounds__(kHeadDim) pool_q_kernel(const PageScoreArgs a) {
+// qm[h][d]: block h; the rows go through shared memory in chunks (coalesced,
+// many loads in flight), then thread d adds its column in row order
+constexpr int kPoolRows = 128;
+__global__ void __launch_bounds__(256) pool_q_kernel(const PageScoreArgs a) {
   pdl_wait();
   pdl_trigger();
-  const int h = blockIdx.x, d = threadIdx.x;
+  __shared__ uint4 rows[kPoolRows * kChunksPerRow];       // 128 rows x 64 bf16
+  const int h = blockIdx.x;
   float acc = 0.f;
-  for (int i = 0; i < a.n_q; ++i)
-    acc = __fadd_rn(acc, bf16_at(a.q + ((long long)i * a.heads + h) * kHeadDim + d));
-  a.qm[h * kHeadDim + d] = __fdiv_rn(acc, (float)a.n_q);
+  for (int r0 = 0; r0 < a.n_q; r0 += kPoolRows) {
+    const int nr = min(kPoolRows, a.n_q - r0);
+    for (int i = threadIdx.x; i < nr * kChunksPerRow; i += blockDim.x)
+      rows[i] = __ldg(reinterpret_cast<const uint4*>(
+                          a.q + ((long long)(r0 + i / kChunksPerRow) * a.heads + h) * kHeadDim) +
+                      i % kChunksPerRow);
+    __syncthreads();
+    if (threadIdx.x < kHeadDim) {
+      const uint16_t* base = reinterpret_cast<const uint16_t*>(rows) + threadIdx.x;
+#pragma unroll 8
+      for (int r = 0; r < nr; ++r)
+        acc = __fadd_rn(acc, __uint_as_float((uint32_t)base[r * kHeadDim] << 16));
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x < kHeadDim)
+    a.qm[h * kHeadDim + threadIdx.x] = __fdiv_rn(acc, (float)a.n_q);
 }
 
-// score of visible page e: block e; thread (h, d) pools its key column, then
-// thread 0 adds the products in (h, d) order
-__global__ void __launch_bounds__(256) page_score_kernel(const PageScoreArgs a) {
+// prod[e][h][d] = qm[h][d] * km[h][d] for page e (blockIdx.x), head h
+// (blockIdx.y): the page's plane of head h (len rows of 128 bytes, swizzled) is
+// copied to shared memory, then thread d adds its column in slot order
+__global__ void __launch_bounds__(kHeadDim) pool_k_kernel(const PageScoreArgs a) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float prod[kMaxHeads * kHeadDim];
-  const int e = blockIdx.x;
+  __shared__ uint4 plane[kMaxPageSize * kChunksPerRow];   // up to 256 rows x 64 bf16
+  const int e = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
   int page = 0, len = 0;
   table_entry(a.tbl, e, page, len);
   const bool ok = page >= 0 && page < a.pool.pool_pages && len >= 1 && len <= a.pool.page_size;
-  const int n = a.heads * kHeadDim;
-  for (int hd = threadIdx.x; hd < n; hd += blockDim.x) {
-    const int h = hd / kHeadDim, d = hd % kHeadDim;
-    float km = 0.f;
-    if (ok) {
-      const uint16_t* col = a.pool.base + (long long)page * a.pool.page_elems +
-                            (long long)h * a.pool.page_size * kHeadDim + (d & 7);
-      float acc = 0.f;
-      for (int s = 0; s < len; ++s)
-        acc = __fadd_rn(acc, bf16_at(col + (long long)s * kHeadDim + swizzle_chunk(s, d >> 3) * 8));
-      km = __fdiv_rn(acc, (float)len);
-    }
-    prod[hd] = __fmul_rn(a.qm[hd], km);
+  float km = __int_as_float(0x7fc00000);                  // NaN: ranks lowest
+  if (ok) {
+    const uint4* src = reinterpret_cast<const uint4*>(
+        a.pool.base + (long long)page * a.pool.page_elems + (long long)h * a.pool.page_size * kHeadDim);
+    for (int i = d; i < len * kChunksPerRow; i += blockDim.x) plane[i] = __ldg(src + i);
+  } else if (d == 0) {
+    atomicOr(a.err, kErrPageRange);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    if (!ok) atomicOr(a.err, kErrPageRange);
+  if (ok) {
+    const uint16_t* p = reinterpret_cast<const uint16_t*>(plane) + (d & 7);
     float acc = 0.f;
-    for (int hd = 0; hd < n; ++hd) acc = __fadd_rn(acc, prod[hd]);
-    a.scores[e] = ok ? acc : __int_as_float(0x7fc00000);    // NaN ranks lowest
+#pragma unroll 8
+    for (int s = 0; s < len; ++s)
+      acc = __fadd_rn(acc, __uint_as_float((uint32_t)p[s * kHeadDim + swizzle_chunk(s, d >> 3) * 8]
+                                           << 16));
+    km = __fdiv_rn(acc, (float)len);
+  }
+  a.prod[((long long)e * a.heads + h) * kHeadDim + d] = __fmul_rn(a.qm[h * kHeadDim + d], km);
+}
+
+// score of page e (block e): the products in (h, d) order, one running sum
+__global__ void __launch_bounds__(256) page_score_kernel(const PageScoreArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ __align__(16) float prod[kMaxHeads * kHeadDim];
+  const int e = blockIdx.x, n = a.heads * kHeadDim;   // a multiple of 64
+  for (int i = threadIdx.x; i < n; i += blockDim.x) prod[i] = a.prod[(long long)e * n + i];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // the loads run ahead four at a time; the adds stay in order
+    const float4* p4 = reinterpret_cast<const float4*>(prod);
+    float acc = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < n / 4; ++i) {
+      const float4 v = p4[i];
+      acc = __fadd_rn(acc, v.x);
+      acc = __fadd_rn(acc, v.y);
+      acc = __fadd_rn(acc, v.z);
+      acc = __fadd_rn(acc, v.w);
+    }
+    a.scores[e] = acc;
   }
 }
 
@@ -104,10 +144,12 @@ __global__ void __launch_bounds__(kMaxSampledEntries) select_kernel(const PageSc
 }  // namespace
 
 cudaError_t launch_page_select(const PageScoreArgs& a, cudaStream_t s) {
-  cudaError_t e = launch_pdl(pool_q_kernel, dim3(a.heads), dim3(kHeadDim), 0, s, a);
+  cudaError_t e = launch_pdl(pool_q_kernel, dim3(a.heads), dim3(256), 0, s, a);
+  if (e == cudaSuccess)
+    e = launch_pdl(pool_k_kernel, dim3(a.n_entries, a.heads), dim3(kHeadDim), 0, s, a);
   if (e == cudaSuccess) e = launch_pdl(page_score_kernel, dim3(a.n_entries), dim3(256), 0, s, a);
   if (e == cudaSuccess) e = launch_pdl(select_kernel, dim3(1), dim3(kMaxSampledEntries), 0, s, a);
-  count_launches(3);
+  count_launches(4);
   return e;
 }
 
