@@ -94,33 +94,45 @@ typedef struct {
 } pkv_stream_cfg;
 
 /* Create a cache of `pool_pages` pages of `page_size` slots for one layer.
- * Equivalent to pkv_create_ex(pool_pages, page_size, heads, head_dim, 1, 64, out). */
+ * Equivalent to pkv_create_ex(pool_pages, page_size, heads, head_dim, 1, 64, out).
+ * Errors: as pkv_create_ex. */
 pkv_status pkv_create(int pool_pages, int page_size, int heads, int head_dim, pkv_t* out);
 
 /* Create with `layers` page sets (one per transformer layer; all layers share one
  * page table, so a page id names the same page in every layer) and room for
  * `max_streams` concurrent streams sharing the pool and its free list.
  * Allocates layers*pool_pages*2*heads*page_size*head_dim bf16 (zeroed). The free
- * list is a stack that initially hands out pages 0, 1, 2, ... */
+ * list is a stack that initially hands out pages 0, 1, 2, ... *out receives the
+ * handle, which the caller releases with pkv_destroy.
+ * Errors: INVALID (null out; head_dim != 64; page_size not a multiple of 16 in
+ * 16..256 that divides or is divisible by 64; pool_pages, heads (<= 32), layers or
+ * max_streams (<= 1024) out of range); OOM or CUDA if the device allocations fail
+ * (nothing is left allocated). The message is pkv_last_error(NULL). */
 pkv_status pkv_create_ex(int pool_pages, int page_size, int heads, int head_dim, int layers,
                          int max_streams, pkv_t* out);
 
-/* Free everything. Synchronises the device first. NULL is accepted. */
+/* Free everything. Synchronises the device first. NULL is accepted. Always OK. */
 pkv_status pkv_destroy(pkv_t h);
 
 /* Open a stream; *stream_id receives the lowest unused id. Allocates the stream's
- * page-id lists on the device (synchronously). */
+ * page-id lists on the device (synchronously).
+ * Errors: INVALID (null argument, a configuration field out of range: frame mode
+ * needs n_patch == page_size, 1 <= n_special <= page_size, window >= 1,
+ * overlap_keyframes <= num_scale; chunked mode 1 <= sliding_window_num <= 16),
+ * OOM (max_streams already open), CUDA (the allocation failed). */
 pkv_status pkv_stream_open(pkv_t h, const pkv_stream_cfg* cfg, int* stream_id);
 
 /* Close a stream: its pages go back on the free stack (frame mode: scale pages,
  * window pages oldest first, then special pages in order; chunked mode: chunks
- * oldest first, pages in order). */
+ * oldest first, pages in order). Synchronises cuda_stream before freeing the
+ * stream's device lists. Errors: INVALID (the stream is not open), CUDA. */
 pkv_status pkv_stream_close(pkv_t h, int stream_id, void* cuda_stream);
 
 /* Return every page of the stream to the free stack (in pkv_stream_close's
  * order) and clear its counters, keeping the stream open and its device lists
  * allocated: the stream starts over as if just opened. No allocation and no
- * synchronisation, so it can sit inside a captured CUDA graph. */
+ * synchronisation, so it can sit inside a captured CUDA graph.
+ * Errors: INVALID (the stream is not open), CUDA (the launch failed). */
 pkv_status pkv_stream_reset(pkv_t h, int stream_id, void* cuda_stream);
 
 /* Append one frame's K and V ("LingBot-Map Paged KV Cache", section 2; RFC
@@ -212,7 +224,9 @@ pkv_status pkv_attend(pkv_t h, const void* q, int n_q, int stream_id, int layer,
 
 /* Chunked-mode attention (RFC 2.3 / 3.3): the current chunk's n_q tokens (n_q
  * must equal the tokens appended to the open chunk) attend over the visible
- * chunks. Same layouts and numerics as pkv_attend. */
+ * chunks. Same layouts and numerics as pkv_attend.
+ * Errors: as pkv_attend; STATE for a frame-mode stream or no open chunk; INVALID
+ * when n_q differs from the open chunk's tokens. */
 pkv_status pkv_attend_chunked(pkv_t h, const void* q, int n_q, int stream_id, int layer,
                               void* out, float sm_scale, void* cuda_stream);
 
@@ -327,7 +341,8 @@ pkv_status pkv_attend_noalloc(pkv_t h, const void* q, int n_q, int stream_id, in
  * pending CUDA error (PKV_ERR_CUDA). */
 pkv_status pkv_sync(pkv_t h, void* cuda_stream);
 
-/* Host-side counts of the stream's visible table (no device access). */
+/* Host-side counts of the stream's visible table (no device access).
+ * Errors: INVALID (the stream is not open, or a null pointer). */
 pkv_status pkv_visible_count(pkv_t h, int stream_id, int* n_pages, int* n_tokens);
 
 /* Number of free pages (host mirror of the free-stack depth). */
@@ -338,12 +353,14 @@ pkv_status pkv_free_pages(pkv_t h, int* n_free);
  *   then the stream's visible table: n, idx[0..n), len[0..n),
  *   then mode-specific counters: frame mode {n_scale, n_window, n_special, sp_len,
  *   kept, pending}; chunked mode {n_chunks, open, pending, tokens of each chunk}.
- * cap_words is the capacity of host_buf; *used_words receives the count. */
+ * cap_words is the capacity of host_buf; *used_words receives the count.
+ * Errors: INVALID (stream not open, null pointer, cap_words too small), CUDA. */
 pkv_status pkv_export_state(pkv_t h, int stream_id, int32_t* host_buf, size_t cap_words,
                             size_t* used_words);
 
 /* Debug / test read of one page's K (kv = 0) or V (kv = 1) of one layer, copied to
- * host_dst as plain bf16 [heads][page_size][64] (un-swizzled). Synchronous. */
+ * host_dst as plain bf16 [heads][page_size][64] (un-swizzled). Synchronous.
+ * Errors: INVALID (null pointer; layer, page or kv out of range), CUDA. */
 pkv_status pkv_read_page(pkv_t h, int layer, int page, int kv, void* host_dst);
 
 /* Synthetic input generator (not part of the cache): fills dst, a device bf16
@@ -351,7 +368,9 @@ pkv_status pkv_read_page(pkv_t h, int layer, int page, int kv, void* host_dst);
  * values of frames frame0 .. frame0+n_frames-1: splitmix64 of the packed key
  * (seed, workload, stream, layer, frame, tensor, token0+t, head, d), four 16-bit
  * uniforms summed, centred, scaled by sqrt(3)*2^-16 in fp32, times `scale` (a
- * power of two), rounded to bf16. */
+ * power of two), rounded to bf16.
+ * Errors: INVALID (a field outside its key bits, a null dst, a scale
+ * that is not a power of two; the message is pkv_last_error(NULL)), CUDA. */
 pkv_status pkv_synth_fill(void* dst, int n_frames, int n_tokens, int heads, int head_dim,
                           int seed, int workload, int stream, int layer, int frame0, int tensor,
                           int token0, float scale, void* cuda_stream);

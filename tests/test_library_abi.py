@@ -70,3 +70,18 @@ def test_null_handle_is_rejected_without_gpu(lib):
     assert L.pkv_attend_sampled(None, None, 1, 0, 0, None, f, 1, 1, None) == 1
     assert L.pkv_evict_window(None, 0, None) == 1
     assert L.pkv_rollback_last_frame(None, 0, None) == 1
+
+
+def test_every_declaration_documents_its_errors():
+    """Each entry point in include/pkv.h sits under a comment that states its
+    error behaviour (the two that cannot fail excepted)."""
+    import re
+    h = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    for m in re.finditer(r"\n(?:pkv_status|const char\*|unsigned long long)\s+(pkv_\w+)\(", h):
+        name = m.group(1)
+        before = h[:m.start()]
+        end = before.rfind("*/")
+        assert end > before.rfind(";"), f"{name}: no comment above the declaration"
+        block = before[before.rfind("/*", 0, end):end]
+        if name not in ("pkv_last_error", "pkv_kernel_launches"):
+            assert "rror" in block or "Always OK" in block, f"{name}: error behaviour not stated"
