@@ -804,10 +804,17 @@ def run_ours(args):
         "clocks": clocks.summary(),
     }
     if not args.no_extra:
-        line["extra"] = {"chunked": extra_chunked(), "long24": extra_long24(), "append": extra_append(),
-                         "multistream": extra_multistream(), "sampled": extra_sampled(),
-                         "frames": extra_frames(), "model24": extra_long24(frame_attn=True),
-                         "blocksparse": extra_blocksparse()}
+        # an extra that fails is reported as such; it does not cost the line
+        def measured(fn, *a, **kw):
+            try:
+                return fn(*a, **kw)
+            except Exception as exc:                    # noqa: BLE001
+                return {"error": "%s: %s" % (type(exc).__name__, str(exc)[:200])}
+        line["extra"] = {"chunked": measured(extra_chunked), "long24": measured(extra_long24),
+                         "append": measured(extra_append), "multistream": measured(extra_multistream),
+                         "sampled": measured(extra_sampled), "frames": measured(extra_frames),
+                         "model24": measured(extra_long24, frame_attn=True),
+                         "blocksparse": measured(extra_blocksparse)}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)
