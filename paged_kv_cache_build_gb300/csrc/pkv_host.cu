@@ -780,6 +780,13 @@ static size_t partial_bytes(const AttendArgs& a) {
   return (size_t)a.num_splits * a.n_q * a.heads * (kHeadDim + 2) * sizeof(float);
 }
 
+// The same rounded up to 256 bytes: the partials of several calls placed back to
+// back each start 16-byte aligned (the kernels move O partials in 16-byte vectors,
+// and splits x n_q x heads x 264 bytes is only a multiple of 8 when all three are odd).
+static size_t partial_bytes_aligned(const AttendArgs& a) {
+  return (partial_bytes(a) + 255) & ~static_cast<size_t>(255);
+}
+
 // Split-KV partials of `a` at `base`: O first, then the (max, sum) pairs.
 static void place_partials(AttendArgs* a, float* base) {
   a->part_o = base;
@@ -1084,7 +1091,7 @@ pkv_status pkv_attend_batched(pkv_t h, const void* q, const int* q_off, const in
     for (int i = 0; i < n; ++i)
       if (shape[i] == sh) {
         calls[i].num_splits = splits_of_shape[sh];
-        if (calls[i].num_splits > 1) scratch += partial_bytes(calls[i]);
+        if (calls[i].num_splits > 1) scratch += partial_bytes_aligned(calls[i]);
       }
   }
   if (scratch > 0) {
@@ -1093,7 +1100,7 @@ pkv_status pkv_attend_batched(pkv_t h, const void* q, const int* q_off, const in
     for (int i = 0; i < n; ++i)
       if (calls[i].num_splits > 1) {
         place_partials(&calls[i], base);
-        base += partial_bytes(calls[i]) / sizeof(float);
+        base += partial_bytes_aligned(calls[i]) / sizeof(float);
       }
   }
   std::unique_ptr<AttendBatch> b(new AttendBatch);
