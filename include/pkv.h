@@ -209,7 +209,8 @@ pkv_status pkv_stream_frames(pkv_t h, int stream_id, int layer, const void* q, c
  * mode: chunks oldest first, pages in order.
  * d_idx, d_len: device int32[capacity] receiving page ids and valid slot counts;
  * d_n, d_last_page_len: device int32 scalars (may be NULL) receiving the entry
- * count and the last entry's length. Errors: INVALID if capacity is too small. */
+ * count and the last entry's length. Errors: INVALID if capacity is too small or a
+ * buffer is null or not 4-byte aligned. */
 pkv_status pkv_build_visible_page_table(pkv_t h, int stream_id, int32_t* d_idx, int32_t* d_len,
                                         int capacity, int32_t* d_n, int32_t* d_last_page_len,
                                         void* cuda_stream);
@@ -369,7 +370,7 @@ pkv_status pkv_read_page(pkv_t h, int layer, int page, int kv, void* host_dst);
  * (seed, workload, stream, layer, frame, tensor, token0+t, head, d), four 16-bit
  * uniforms summed, centred, scaled by sqrt(3)*2^-16 in fp32, times `scale` (a
  * power of two), rounded to bf16.
- * Errors: INVALID (a field outside its key bits, a null dst, a scale
+ * Errors: INVALID (a field outside its key bits, a null or odd dst, a scale
  * that is not a power of two; the message is pkv_last_error(NULL)), CUDA. */
 pkv_status pkv_synth_fill(void* dst, int n_frames, int n_tokens, int heads, int head_dim,
                           int seed, int workload, int stream, int layer, int frame0, int tensor,

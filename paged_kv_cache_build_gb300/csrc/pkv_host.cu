@@ -728,6 +728,9 @@ pkv_status pkv_build_visible_page_table(pkv_t h, int sid, int32_t* d_idx, int32_
   int np, nt, last;
   visible_counts(h, *st, &np, &nt, &last);
   if (np > 0 && (!d_idx || !d_len)) return fail(h, PKV_ERR_INVALID, "null table buffers");
+  const auto misaligned4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; };
+  if (misaligned4(d_idx) || misaligned4(d_len) || misaligned4(d_n) || misaligned4(d_last_page_len))
+    return fail(h, PKV_ERR_INVALID, "table buffers must be 4-byte aligned");
   if (capacity < np) return fail(h, PKV_ERR_INVALID, "capacity %d < %d entries", capacity, np);
   TableArgs t = table_args(h, *st, d_idx, d_len, d_n, d_last_page_len);
   PKV_CUDA(h, launch_table(t, as_stream(cuda_stream)));
@@ -1217,6 +1220,8 @@ pkv_status pkv_synth_fill(void* dst, int n_frames, int n_tokens, int heads, int 
       stream >= 64 || layer < 0 || layer >= 32 || frame0 < 0 || frame0 + n_frames > 65536 ||
       tensor < 0 || tensor >= 4 || token0 < 0 || token0 + n_tokens > 16384)
     return fail(nullptr, PKV_ERR_INVALID, "pkv_synth_fill: argument out of range");
+  if (reinterpret_cast<uintptr_t>(dst) & 1u)
+    return fail(nullptr, PKV_ERR_INVALID, "pkv_synth_fill: dst must be 2-byte aligned");
   int e2;
   const float m = std::frexp(scale, &e2);
   if (m != 0.5f) return fail(nullptr, PKV_ERR_INVALID, "pkv_synth_fill: scale must be a power of two");

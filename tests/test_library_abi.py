@@ -85,3 +85,10 @@ def test_every_declaration_documents_its_errors():
         block = before[before.rfind("/*", 0, end):end]
         if name not in ("pkv_last_error", "pkv_kernel_launches"):
             assert "rror" in block or "Always OK" in block, f"{name}: error behaviour not stated"
+
+
+def test_misaligned_generator_target_is_rejected_without_gpu(lib):
+    from paged_kv_cache_build_gb300._lib import load
+    L = load()
+    assert L.pkv_synth_fill(ctypes.c_void_p(0x1001), 1, 1, 1, 64, 0, 0, 0, 0, 0, 0, 0, 1.0, None) == 1
+    assert b"2-byte aligned" in L.pkv_last_error(None)
