@@ -803,7 +803,7 @@ def run_ours(args):
         "launches_per_step": int(per_step_launches),
         "clocks": clocks.summary(),
     }
-    if not args.no_extra:
+    if not args.no_extra and world == 1:
         # an extra that fails is reported as such; it does not cost the line
         def measured(fn, *a, **kw):
             try:
@@ -815,7 +815,7 @@ def run_ours(args):
                          "sampled": measured(extra_sampled), "frames": measured(extra_frames),
                          "model24": measured(extra_long24, frame_attn=True),
                          "blocksparse": measured(extra_blocksparse)}
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:      # the host baseline: N = 1 only
         line["cpu_baseline"] = oracle_sample(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)
 
