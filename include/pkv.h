@@ -93,13 +93,17 @@ typedef struct {
   int tokens_per_frame;  /* tokens appended per frame (1374)                        */
 } pkv_stream_cfg;
 
-/* Create a cache of `pool_pages` pages of `page_size` slots for one layer.
+/* Create a cache of `pool_pages` pages of `page_size` slots for one layer
+ * ("LingBot-Map Paged KV Cache", section 2: each layer's KV lives in fixed-size
+ * pages handed out from a free list).
  * Equivalent to pkv_create_ex(pool_pages, page_size, heads, head_dim, 1, 64, out).
  * Errors: as pkv_create_ex. */
 pkv_status pkv_create(int pool_pages, int page_size, int heads, int head_dim, pkv_t* out);
 
-/* Create with `layers` page sets (one per transformer layer; all layers share one
- * page table, so a page id names the same page in every layer) and room for
+/* Create with `layers` page sets ("LingBot-Map Paged KV Cache", section 2: the
+ * cache is kept per layer, in fixed-size pages taken from a free list; here all
+ * layers share one page table, so a page id names the same page in every layer,
+ * and the metadata is updated once per frame) and room for
  * `max_streams` concurrent streams sharing the pool and its free list.
  * Allocates layers*pool_pages*2*heads*page_size*head_dim bf16 (zeroed). The free
  * list is a stack that initially hands out pages 0, 1, 2, ... *out receives the
@@ -114,8 +118,16 @@ pkv_status pkv_create_ex(int pool_pages, int page_size, int heads, int head_dim,
 /* Free everything. Synchronises the device first. NULL is accepted. Always OK. */
 pkv_status pkv_destroy(pkv_t h);
 
-/* Open a stream; *stream_id receives the lowest unused id. Allocates the stream's
- * page-id lists on the device (synchronously).
+/* Open a stream; *stream_id receives the lowest unused id ("LingBot-Map Paged KV
+ * Cache", section 2: a stream's cache is its scale, sliding-window and special
+ * page lists, filled from the shared free list; section 4: windowed mode; vLLM-Omni
+ * RFC "Reconstruction Engine", sections 2.3 and 3.3: a chunked stream keeps the
+ * pages of its most recent sliding_window_num chunks). Allocates the stream's
+ * page-id lists on the device (synchronously), and grows the handle's split-KV
+ * scratch to what this stream's attention calls need at their natural query
+ * count (frame mode: n_patch + n_special rows; chunked mode: chunk_size x
+ * tokens_per_frame rows) for every table size the stream can reach, so that
+ * those calls never allocate.
  * Errors: INVALID (null argument, a configuration field out of range: frame mode
  * needs n_patch == page_size, 1 <= n_special <= page_size, window >= 1,
  * overlap_keyframes <= num_scale; chunked mode 1 <= sliding_window_num <= 16),
@@ -146,8 +158,10 @@ pkv_status pkv_stream_reset(pkv_t h, int stream_id, void* cuda_stream);
  * scattered into their slots. layer > 0 writes the same slots of that layer's
  * page set and must follow layer 0 of the same frame.
  * Errors: INVALID (shape / layer), OOM (too few free pages), STATE (frame mode:
- * the window already holds `window` pages; chunked: the chunk is full or the
- * window holds sliding_window_num chunks; layer > 0 without a pending frame). */
+ * the window already holds `window` pages, or layer == 0 while the previous frame
+ * is still pending, i.e. neither rolled back nor committed by pkv_evict_window;
+ * chunked: the chunk is full or the window holds sliding_window_num chunks;
+ * layer > 0 without a pending frame). */
 pkv_status pkv_append_frame(pkv_t h, int stream_id, int layer, const void* k, const void* v,
                             int n_tokens, void* cuda_stream);
 
@@ -328,9 +342,10 @@ pkv_status pkv_attend_batched(pkv_t h, const void* q, const int* q_off, const in
  *  - A call whose partial results need more than 16 MiB (num_splits x n_q x heads
  *    x 264 bytes; e.g. a whole 8 x 1374-token chunk) returns PKV_ERR_INVALID and
  *    launches nothing.
- *  - The first call on a device resolves the array's device address
- *    (cudaGetSymbolAddress) for that device; make that first call before any
- *    stream capture.
+ *  - pkv_create_ex resolves the array's device address (cudaGetSymbolAddress,
+ *    no allocation) for the device current at creation, which is the handle's
+ *    device; a handle created after a device reset resolves it again. So the
+ *    set-up happens once per handle, before any stream capture of its calls.
  *  - Every call, on every handle and stream, shares the one array, which keeps
  *    the last call's contents (nothing in it needs to start at zero: each call
  *    writes every partial it reads). Calls that overlap on the GPU race: order
@@ -378,6 +393,13 @@ pkv_status pkv_synth_fill(void* dst, int n_frames, int n_tokens, int heads, int 
 
 /* Kernels this library has launched in the calling process so far (all handles). */
 unsigned long long pkv_kernel_launches(void);
+
+/* The handle's split-KV scratch: its current size in bytes and how many times it
+ * has been (re)allocated. pkv_stream_open sizes it for the stream's natural query
+ * count; a later attention call that needs more (another query count, or a
+ * batched call) grows it, which synchronises the device and allocates.
+ * Errors: INVALID (null argument). */
+pkv_status pkv_scratch_info(pkv_t h, size_t* bytes, int* allocs);
 
 /* Message of the last error on this handle ("" if none). h may be NULL for
  * errors of pkv_create. */

@@ -59,6 +59,7 @@ SIGNATURES = {
     "pkv_synth_fill": (c_int, [c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                c_int, c_int, c_int, c_float, c_void_p]),
     "pkv_kernel_launches": (ctypes.c_ulonglong, []),
+    "pkv_scratch_info": (c_int, [c_void_p, ctypes.POINTER(c_size_t), ctypes.POINTER(c_int)]),
     "pkv_last_error": (ctypes.c_char_p, [c_void_p]),
 }
 

@@ -229,6 +229,12 @@ class PagedKVCache:
         self._check(self.lib.pkv_visible_count(self.h, sid, ctypes.byref(n_pages), ctypes.byref(n_tokens)))
         return n_pages.value, n_tokens.value
 
+    def scratch_info(self):
+        """(bytes, allocations) of the handle's split-KV scratch."""
+        b, n = ctypes.c_size_t(), ctypes.c_int()
+        self._check(self.lib.pkv_scratch_info(self.h, ctypes.byref(b), ctypes.byref(n)))
+        return b.value, n.value
+
     def free_pages(self):
         n = ctypes.c_int()
         self._check(self.lib.pkv_free_pages(self.h, ctypes.byref(n)))

@@ -42,6 +42,7 @@
 // returning.
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "pkv_internal.cuh"
@@ -917,12 +918,17 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
 template <int MT, bool EXTRA, typename Params>
 cudaError_t launch_mt(const Params& p, int grid, int n_mgroups, int n_tiles, cudaStream_t s) {
   const size_t smem = sizeof(TcSmem<MT>) + 1024;
-  static bool configured = false;
-  if (!configured) {
+  // the shared-memory opt-in is a per-device function attribute: set it once for
+  // every device this process launches on
+  static std::atomic<unsigned long long> configured{0};
+  int dev = 0;
+  if (cudaError_t e = cudaGetDevice(&dev)) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (dev >= 64 || !(configured.load() & bit)) {
     cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<MT, EXTRA, Params>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    if (dev < 64) configured.fetch_or(bit);
   }
   const cudaError_t e = launch_pdl(attend_tc_kernel<MT, EXTRA, Params>, dim3(grid),
                                    dim3(tc_threads<MT, EXTRA>()), smem, s, p, n_mgroups, n_tiles);

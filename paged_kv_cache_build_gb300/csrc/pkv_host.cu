@@ -17,7 +17,6 @@
 #include <cstdio>
 #include <cstring>
 #include <memory>
-#include <mutex>
 #include <string>
 #include <vector>
 
@@ -67,6 +66,9 @@ struct pkv_ctx {
   std::vector<Stream> streams;
   float* d_scratch = nullptr;
   size_t scratch_bytes = 0;
+  int scratch_allocs = 0;        // times the split-KV scratch was (re)allocated
+  int device = 0;                // the device current at pkv_create_ex
+  float* noalloc_scratch = nullptr;   // device address of the static scratch on `device`
   void* d_select = nullptr;      // page skipping: query means, page estimates, kept list
   int select_kept = 0;           // entries in that kept list (the last call's)
   int num_sms = 0;
@@ -76,6 +78,12 @@ struct pkv_ctx {
 namespace {
 
 std::string g_create_error;
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;   // 16 MiB
+// The partial (o, m, l) results of pkv_attend_noalloc, shared by every call on
+// every handle. In host code this name is only a stand-in for the symbol: kernels
+// get the device address that pkv_create_ex resolves with cudaGetSymbolAddress.
+static __device__ __align__(256) float g_noalloc_scratch[kStaticScratchBytes / sizeof(float)];
 
 pkv_status fail(pkv_t h, pkv_status st, const char* fmt, ...) {
   char buf[512];
@@ -220,6 +228,13 @@ extern "C" {
 
 unsigned long long pkv_kernel_launches(void) { return pkv::launch_count(); }
 
+pkv_status pkv_scratch_info(pkv_t h, size_t* bytes, int* allocs) {
+  if (!h || !bytes || !allocs) return fail(h, PKV_ERR_INVALID, "null argument");
+  *bytes = h->scratch_bytes;
+  *allocs = h->scratch_allocs;
+  return PKV_OK;
+}
+
 const char* pkv_last_error(pkv_t h) { return h ? h->last_error.c_str() : g_create_error.c_str(); }
 
 pkv_status pkv_create(int pool_pages, int page_size, int heads, int head_dim, pkv_t* out) {
@@ -249,7 +264,14 @@ pkv_status pkv_create_ex(int pool_pages, int page_size, int heads, int head_dim,
   h->streams.resize(max_streams);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
+  h->device = dev;
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) {
+    // the static scratch of pkv_attend_noalloc on this device (no allocation)
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    h->noalloc_scratch = static_cast<float*>(p);
+  }
   const size_t pool_bytes = (size_t)layers * pool_pages * h->page_elems * sizeof(uint16_t);
   if (e == cudaSuccess) e = cudaMalloc(&h->d_pool, pool_bytes);
   if (e == cudaSuccess) e = cudaMemset(h->d_pool, 0, pool_bytes);
@@ -286,6 +308,48 @@ pkv_status pkv_destroy(pkv_t h) {
   delete h;
   return PKV_OK;
 }
+
+}  // extern "C"
+
+namespace {
+
+pkv_status ensure_scratch(pkv_t h, size_t bytes) {
+  if (bytes <= h->scratch_bytes) return PKV_OK;
+  PKV_CUDA(h, cudaDeviceSynchronize());
+  if (h->d_scratch) cudaFree(h->d_scratch);
+  h->d_scratch = nullptr;
+  h->scratch_bytes = 0;
+  PKV_CUDA(h, cudaMalloc(&h->d_scratch, bytes));
+  h->scratch_bytes = bytes;
+  h->scratch_allocs++;
+  return PKV_OK;
+}
+
+// Split-KV scratch that the attention calls of a stream with this configuration
+// need at their natural query count (a frame's n_patch + n_special rows, or a
+// whole chunk), for the largest split count any reachable table size gives.
+size_t stream_scratch_need(const pkv_ctx* h, const pkv_stream_cfg& c) {
+  long long n_q = 0, max_slots = 0;
+  if (c.mode == PKV_MODE_FRAME) {
+    n_q = (long long)c.n_patch + c.n_special;
+    max_slots = ((long long)c.num_scale + c.window + h->P) * h->Ps;
+  } else {
+    const long long chunk = (long long)c.chunk_size * c.tokens_per_frame;
+    n_q = chunk;
+    max_slots = (long long)c.sliding_window_num * ceil_div(chunk, h->Ps) * h->Ps;
+  }
+  if (n_q > (1 << 20)) return 0;
+  const int max_tiles = attend_tc_tiles(max_slots);
+  int max_splits = 1;
+  for (int t = 1; t <= max_tiles; ++t)
+    max_splits = std::max(max_splits, attend_tc_splits((int)n_q, h->H, t, h->num_sms));
+  if (max_splits == 1) return 0;
+  return (size_t)max_splits * n_q * h->H * (kHeadDim + 2) * sizeof(float);
+}
+
+}  // namespace
+
+extern "C" {
 
 pkv_status pkv_stream_open(pkv_t h, const pkv_stream_cfg* cfg, int* stream_id) {
   if (!h || !cfg || !stream_id) return fail(h, PKV_ERR_INVALID, "null argument");
@@ -328,6 +392,7 @@ pkv_status pkv_stream_open(pkv_t h, const pkv_stream_cfg* cfg, int* stream_id) {
       break;
     }
   if (sid < 0) return fail(h, PKV_ERR_OOM, "no free stream id");
+  if (pkv_status r = ensure_scratch(h, stream_scratch_need(h, c))) return r;
   cudaError_t e = cudaMalloc(&st.d_mem, words * sizeof(int32_t));
   if (e != cudaSuccess) return cuda_fail(h, e, "stream_open cudaMalloc");
   e = cudaMemset(st.d_mem, 0, words * sizeof(int32_t));
@@ -469,6 +534,9 @@ static pkv_status append_chunked(pkv_t h, Stream* st, int layer, const void* k, 
 static pkv_status plan_frame_append(pkv_t h, Stream* st, const void* k, const void* v,
                                     AppendItem* it, int* need) {
   const pkv_stream_cfg& c = st->cfg;
+  if (st->pending)
+    return fail(h, PKV_ERR_STATE,
+                "a frame is pending: roll it back or commit it with pkv_evict_window first");
   const bool to_scale = st->n_scale < c.num_scale;
   if (!to_scale && st->win_count == c.window)
     return fail(h, PKV_ERR_STATE, "window is full: evict before appending");
@@ -734,17 +802,6 @@ pkv_status pkv_build_visible_page_table(pkv_t h, int sid, int32_t* d_idx, int32_
   if (capacity < np) return fail(h, PKV_ERR_INVALID, "capacity %d < %d entries", capacity, np);
   TableArgs t = table_args(h, *st, d_idx, d_len, d_n, d_last_page_len);
   PKV_CUDA(h, launch_table(t, as_stream(cuda_stream)));
-  return PKV_OK;
-}
-
-static pkv_status ensure_scratch(pkv_t h, size_t bytes) {
-  if (bytes <= h->scratch_bytes) return PKV_OK;
-  PKV_CUDA(h, cudaDeviceSynchronize());
-  if (h->d_scratch) cudaFree(h->d_scratch);
-  h->d_scratch = nullptr;
-  h->scratch_bytes = 0;
-  PKV_CUDA(h, cudaMalloc(&h->d_scratch, bytes));
-  h->scratch_bytes = bytes;
   return PKV_OK;
 }
 
@@ -1242,29 +1299,13 @@ pkv_status pkv_synth_fill(void* dst, int n_frames, int n_tokens, int heads, int 
 
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(16) << 20;   // 16 MiB
-// The partial (o, m, l) results of pkv_attend_noalloc, shared by every call on
-// every handle. In host code this name is only a stand-in for the symbol: kernels
-// get the device address resolved by cudaGetSymbolAddress below.
-static __device__ __align__(256) float g_noalloc_scratch[kStaticScratchBytes / sizeof(float)];
-
-constexpr int kMaxDevices = 64;
-float* g_noalloc_ptr[kMaxDevices] = {nullptr};
-std::mutex g_noalloc_mu;
-
-// Device address of the static scratch on the current device, resolved once per
-// device (with that device current).
+// Device address of the static scratch for the handle's device. pkv_create_ex
+// resolved it with that device current; a handle created after a device reset
+// resolves it again.
 pkv_status noalloc_scratch(pkv_t h, float** out) {
-  int dev = 0;
-  PKV_CUDA(h, cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kMaxDevices) return fail(h, PKV_ERR_INVALID, "device %d out of range", dev);
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    PKV_CUDA(h, cudaGetSymbolAddress(&p, g_noalloc_scratch));
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_noalloc_ptr[dev];
+  if (!h->noalloc_scratch)
+    return fail(h, PKV_ERR_CUDA, "the static scratch's device address could not be resolved");
+  *out = h->noalloc_scratch;
   return PKV_OK;
 }
 

@@ -124,6 +124,25 @@ class Pair:
         return o, e_abs_v
 
 
+def oracle_attention_all_rows(pair, sid, layer, q_bits, block=1374, workers=8):
+    """Pair.oracle_attention over every query row, the rows cut into blocks that
+    threads compute side by side (the oracle itself is unchanged: each block is
+    one call of attend_fp64 with its `rows`)."""
+    from concurrent.futures import ThreadPoolExecutor
+    k, v = gather_visible(pair.ora.visible_tokens(sid), layer, pair.lookup)
+    v_abs = v & np.uint16(0x7FFF)
+    n = q_bits.shape[0]
+    blocks = [np.arange(r, min(n, r + block)) for r in range(0, n, block)]
+
+    def one(rows):
+        return (attend_fp64(q_bits, k, v, pair.w.sm_scale, rows=rows),
+                attend_fp64(q_bits, k, v_abs, pair.w.sm_scale, rows=rows))
+
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        parts = list(ex.map(one, blocks))
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
+
+
 def assert_close(gpu_out, oracle_out, e_abs_v, what=""):
     """The required max/mean tolerance, plus the bound derived from the arithmetic.
     bf16 has an 8-bit significand, so round-to-nearest is off by at most 2^-8

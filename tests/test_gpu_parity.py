@@ -13,7 +13,7 @@ import pytest
 import torch
 
 from synth import TENSOR_K, TENSOR_Q, TENSOR_V, WORKLOADS, frame_tensor, is_keyframe, multistream_schedule
-from tests.pairing import Pair, assert_close
+from tests.pairing import Pair, assert_close, oracle_attention_all_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -245,8 +245,9 @@ def test_long_stream_keyframes_24_layers():
 
 def test_chunked_vggt_stream():
     """RFC chunked sliding-window attention: 64 chunks of 8 x 1374 tokens, 4
-    chunks visible; tables every chunk, attention of chunks 0-3 and 63 on every
-    16th query row."""
+    chunks visible; tables every chunk, attention of chunks 0-2 and 63 on every
+    16th query row, and of chunk 3 (the first with all 4 chunks visible: 43 M-groups
+    x 16 heads x 3 KV splits) on all 10,992 query rows."""
     w = WORKLOADS["chunked"]
     n_chunks = int(os.environ.get("PKV_CHUNKS", 64))
     pr = Pair(w)
@@ -259,7 +260,10 @@ def test_chunked_vggt_stream():
         pr.check_meta(sid)
         q = pr.gpu_q_chunk(sid, 0, frames)
         out = pr.gpu.attend_chunked(q, sid, 0, sm_scale=w.sm_scale)
-        if c in check:
+        if c == 3:
+            o, e = oracle_attention_all_rows(pr, sid, 0, pr.cpu_q(sid, 0, frames))
+            assert_close(out, o, e, f"chunk {c}, all rows")
+        elif c in check:
             rows = np.arange(0, q.shape[0], 16)
             o, e = pr.oracle_attention(sid, 0, pr.cpu_q(sid, 0, frames), rows=rows)
             assert_close(out[torch.from_numpy(rows).cuda()], o, e, f"chunk {c}")

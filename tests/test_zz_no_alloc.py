@@ -99,3 +99,37 @@ def test_noalloc_rejects_more_than_its_scratch(lib):
     assert torch.isfinite(ref.float()).all()
     cache.sync()
     cache.close()
+
+
+def test_noalloc_chunked_uses_the_static_scratch(lib):
+    """A small chunked stream (chunks of 2 x 300 tokens, 4 visible, 4 heads,
+    64-slot pages) whose whole-chunk call fits the fixed array: every call runs in
+    several KV splits (two launches: the attention and the combine that reads the
+    partials back from the array) and matches pkv_attend_chunked, twice in a row."""
+    from paged_kv_cache_build_gb300 import PagedKVCache, chunked_stream_cfg, kernel_launches
+    w = WORKLOADS["chunked"]
+    heads, tokens, chunk, window = 4, 300, 2, 4
+    cache = PagedKVCache(64, 64, heads, 64)
+    sid = cache.open_stream(chunked_stream_cfg(chunk, window, tokens))
+    kv = torch.empty((2, chunk, tokens, heads, 64), dtype=torch.bfloat16, device="cuda")
+    q = torch.empty((chunk * tokens, heads, 64), dtype=torch.bfloat16, device="cuda")
+    for c in range(6):
+        _fill(kv[0], w, sid, c * chunk, TENSOR_K)
+        _fill(kv[1], w, sid, c * chunk, TENSOR_V)
+        _fill(q.view(chunk, tokens, heads, 64), w, sid, c * chunk, TENSOR_Q)
+        for f in range(chunk):
+            cache.append_frame(sid, kv[0, f], kv[1, f])
+        ref = cache.attend_chunked(q, sid, sm_scale=w.sm_scale)
+        torch.cuda.synchronize()
+        for _ in range(2):
+            got = torch.full_like(q, float("nan"))
+            n0 = kernel_launches()
+            assert _noalloc(lib, cache, q, sid, got, w.sm_scale) == 0, lib.pkv_last_error(cache.h)
+            assert kernel_launches() - n0 == 2          # split: attention + combine
+            torch.cuda.synchronize()
+            mx, mean = _close(got, ref)
+            assert mx <= MAX_ABS and mean <= MEAN_ABS, (c, mx, mean)
+            assert torch.isfinite(got.float()).all()
+        cache.evict_window(sid)
+    cache.sync()
+    cache.close()
