@@ -51,7 +51,8 @@ namespace pkv {
 
 namespace {
 
-constexpr int kBN = 64;            // slots per KV tile
+constexpr int kBN = kTileSlots;    // slots per KV tile (64)
+constexpr int kMaxMaskTiles = 512; // tiles of a CTA whose slot masks are precomputed
 constexpr int kStages = 8;         // KV ring depth
 constexpr int kXRows = 8;          // extra query rows handled with mma.sync
 constexpr int kXWarps = kBN / 16;  // extra-row warps: one 16-slot quarter of a tile each
@@ -76,13 +77,13 @@ struct __align__(1024) TcSmem {
   uint8_t v[kStages][kBN * 128];
   float xo[kXWarps][kXRows][kHeadDim];  // extra rows: each warp's partial O ...
   float xml[kXWarps][kXRows][2];        // ... and its running max and sum
-  uint64_t mask[kStages];            // slot validity of the stage's tile
+  uint64_t tmask[kMaxMaskTiles];     // slot validity of the CTA's tiles (precomputed)
   uint16_t kept[kMaxSampledEntries]; // a sampled call's kept table positions
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[MT][2];            // S_m of the buffer's latest tile is in TMEM
-  uint64_t p_full[MT];               // P_m of the latest tile is in TMEM, S_m read, O_m rescaled
-  uint64_t o_done[MT];               // PV of the latest tile has completed
+  uint64_t p_full[MT][2];            // P_m of tile j is in TMEM, S_m read, O_m rescaled (j & 1)
+  uint64_t o_done[MT];               // PV of the latest tile has completed (waited only to rescale O)
   uint64_t mma_done[MT];
   uint64_t x_done;                   // the extra-row warps have published their partials
   uint32_t tmem_base;
@@ -319,6 +320,31 @@ __device__ __forceinline__ CtaWork cta_work(const AttendDense& d, int n_mgroups,
   return {&d.a, (int)blockIdx.x % per_frame, n_mgroups, n_tiles, (int)blockIdx.x / per_frame};
 }
 
+// Valid slots of a tile (bit i: slot i): dense frames by the frame's token count;
+// paged tables by each page block's valid length, from the table's counters and,
+// for a sampled call, the kept list in shared memory. Reads no device memory
+// beyond the kernel's parameters.
+template <bool kDense>
+__device__ __forceinline__ uint64_t tile_mask(const AttendArgs& a, const uint16_t* kept, int tile) {
+  if (kDense) {
+    const int n = min(kBN, a.n_q - tile * kBN);
+    return n >= kBN ? ~0ull : ((1ull << n) - 1ull);
+  }
+  const int Ps = a.page_size;
+  const int rows = Ps >= kBN ? kBN : Ps;
+  const int per = kBN / rows;
+  uint64_t bits = 0ull;
+  for (int pp = 0; pp < per; ++pp) {
+    const int f0 = tile * kBN + pp * rows;
+    const int e = f0 / Ps, so = f0 - e * Ps;
+    if (e >= a.n_entries) break;
+    int n = table_len(a.tbl, a.sampled ? (int)kept[e] : e) - so;
+    n = n < 0 ? 0 : (n > rows ? rows : n);
+    if (n > 0) bits |= (n == 64 ? ~0ull : ((1ull << n) - 1ull)) << (pp * rows);
+  }
+  return bits;
+}
+
 template <int MT, bool EXTRA, typename Params>
 __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     attend_tc_kernel(const __grid_constant__ Params params, int n_mgroups_1, int n_tiles_1) {
@@ -355,7 +381,8 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     for (int m = 0; m < MT; ++m) {
       mbar_init(&sm.s_full[m][0], 1);
       mbar_init(&sm.s_full[m][1], 1);
-      mbar_init(&sm.p_full[m], 4);                    // one per softmax warp of the M-tile
+      mbar_init(&sm.p_full[m][0], 4);                 // one per softmax warp of the M-tile
+      mbar_init(&sm.p_full[m][1], 4);
       mbar_init(&sm.o_done[m], 1);
       mbar_init(&sm.mma_done[m], 1);
     }
@@ -410,27 +437,39 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     }
     fence_proxy_async();
   }
-  // Visible-table entries for the producer, 32 at a time (one per lane): the
-  // entry lookups are dependent global loads, so a batch costs one latency.
   // A sampled call's kept table positions, in order (producer warp, a ballot
-  // per 32 positions); the producer then indexes the kept pages only.
-  if (warp == kProducerWarp && a.sampled) {
-    if (a.kept_dev) {
-      // a list made on the device (page skipping by estimated mass)
-      for (int i = lane; i < a.n_entries; i += 32) sm.kept[i] = __ldcg(a.kept_dev + i);
-    } else {
-      int count = 0;
-      for (int e0 = 0; e0 < a.n_entries_all; e0 += 32) {
-        const int e = e0 + lane;
-        const bool keep = e < a.n_entries_all &&
-                          (e < a.sample_anchor || page_sample_kept(a.sample_key, e, a.sample_keep));
-        const unsigned ball = __ballot_sync(0xffffffffu, keep);
-        if (keep) sm.kept[count + __popc(ball & ((1u << lane) - 1u))] = (uint16_t)e;
-        count += __popc(ball);
+  // per 32 positions); the producer then indexes the kept pages only, and the
+  // other roles read the list for the tiles' slot masks (hence the CTA barrier).
+  if (a.sampled) {
+    if (warp == kProducerWarp) {
+      if (a.kept_dev) {
+        // a list made on the device (page skipping by estimated mass)
+        for (int i = lane; i < a.n_entries; i += 32) sm.kept[i] = __ldcg(a.kept_dev + i);
+      } else {
+        int count = 0;
+        for (int e0 = 0; e0 < a.n_entries_all; e0 += 32) {
+          const int e = e0 + lane;
+          const bool keep = e < a.n_entries_all &&
+                            (e < a.sample_anchor || page_sample_kept(a.sample_key, e, a.sample_keep));
+          const unsigned ball = __ballot_sync(0xffffffffu, keep);
+          if (keep) sm.kept[count + __popc(ball & ((1u << lane) - 1u))] = (uint16_t)e;
+          count += __popc(ball);
+        }
       }
     }
-    __syncwarp();
+    __syncthreads();
   }
+  // Slot masks of the CTA's tiles, computed once by the roles that read them
+  // (the softmax and extra-row warps), so that the tile loops read neither the
+  // kernel's parameters nor the stage's copy barrier for them.
+  if (warp != kProducerWarp) {
+    constexpr int kThreads = tc_threads<MT, EXTRA>() - 32;
+    const int tt = warp < kProducerWarp ? (int)threadIdx.x : (int)threadIdx.x - 32;
+    for (int j = tt; j < nT && j < kMaxMaskTiles; j += kThreads)
+      sm.tmask[j] = tile_mask<kDense>(a, sm.kept, t0 + j);
+  }
+  // Visible-table entries for the producer, 32 at a time (one per lane): the
+  // entry lookups are dependent global loads, so a batch costs one latency.
   // table position of the producer's e-th entry
   auto entry_of = [&](int e) { return a.sampled ? (int)sm.kept[e] : e; };
   const int e_first = kDense ? 0 : (int)((long long)t0 * kBN / Ps);
@@ -462,9 +501,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
         const int s = j % kStages;
         if (!mbar_wait(&sm.kv_empty[s], ((j / kStages) & 1) ^ 1, abort, a.err)) break;
         const int tile = t0 + j;
-        const int n = min(kBN, a.n_q - tile * kBN);  // >= 1: tile < n_tiles
         if (lane == 0) {
-          sm.mask[s] = n >= kBN ? ~0ull : ((1ull << n) - 1ull);
           const uint32_t mb = smem_u32(&sm.kv_full[s]);
           mbar_arrive_expect_tx(&sm.kv_full[s], 2u * kBN * 128u);
           tma_load_3d(smem_u32(&sm.k[s][0]), &params.k_map, 0, h, kv_row0 + tile * kBN, mb);
@@ -479,7 +516,6 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
       const int s = j % kStages;
       if (!mbar_wait(&sm.kv_empty[s], ((j / kStages) & 1) ^ 1, abort, a.err)) break;
       const int tile = t0 + j;
-      uint64_t bits = 0;
       int nblk = 0, blk_page[kBN / 16], blk_so[kBN / 16];
 #pragma unroll
       for (int pp = 0; pp < kBN / 16; ++pp) {
@@ -492,17 +528,11 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
           e_page = e_len = 0;
           if (e_batch + lane < a.n_entries) table_entry(a.tbl, entry_of(e_batch + lane), e_page, e_len);
         }
-        const int page = __shfl_sync(0xffffffffu, e_page, e - e_batch);
-        const int len = __shfl_sync(0xffffffffu, e_len, e - e_batch);
-        int n = len - so;
-        n = n < 0 ? 0 : (n > rows ? rows : n);
-        if (n > 0) bits |= (n == 64 ? ~0ull : ((1ull << n) - 1ull)) << (pp * rows);
-        blk_page[pp] = page;
+        blk_page[pp] = __shfl_sync(0xffffffffu, e_page, e - e_batch);
         blk_so[pp] = so;
         nblk = pp + 1;
       }
       if (lane == 0) {
-        sm.mask[s] = bits;
         mbar_arrive_expect_tx(&sm.kv_full[s], (uint32_t)nblk * 2u * rows * 128u);
 #pragma unroll
         for (int pp = 0; pp < kBN / 16; ++pp) {
@@ -567,7 +597,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
       bool ok = nT < 1 || issue_qk(0);
       ok = ok && (nT < 2 || issue_qk(1));
       for (int j = 0; ok && j < nT; ++j) {
-        if (!mbar_wait(&sm.p_full[m], j & 1, abort, a.err)) break;
+        if (!mbar_wait(&sm.p_full[m][j & 1], (j >> 1) & 1, abort, a.err)) break;
         tc_fence_after();
         const uint64_t vb = sdesc(smem_u32(&sm.v[j % kStages][0]));
         const uint32_t t_p = tmem + TmemCols<MT>::kP + (kBN / 2) * (2 * m + (j & 1));
@@ -594,33 +624,24 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;          // running max (log2 units) and sum
     bool alive = true;
-    // o_done phases this warp has seen complete. A parity wait on phase n is
-    // exact only while the barrier has completed n or n + 1 phases, so the warp
-    // confirms PV(j-1) at the end of every tile j: PV(j) cannot have started
-    // then (it waits for this warp), and PV(j-1), issued when tile j began, has
-    // normally finished during the exponentials. It also frees the P buffer
-    // that tile j + 1 writes.
-    int o_seen = 0;
-    auto wait_pv = [&](int upto) -> bool {       // PV of tiles 0 .. upto completed
-      for (; o_seen <= upto; ++o_seen)
-        if (!mbar_wait(&sm.o_done[m], o_seen & 1, abort, a.err)) return false;
-      tc_fence_after();
-      return true;
-    };
+    // One wait per tile, for S of the tile. The issuing thread issues QK(j) after
+    // PV(j - 2), and the commit that announces S(j) covers every MMA it issued
+    // before, so S(j) also means that PV(j - 2), the last reader of the P buffer
+    // tile j writes, has completed. PV(j - 1) is waited for only when O must be
+    // rescaled: a parity wait on o_done phase j - 1 is exact during tile j,
+    // since phase j - 2 has completed (S(j)) and phase j cannot start before
+    // this warp arrives. The arrivals of tile j go to p_full[m][j & 1]: a warp
+    // that runs ahead to tile j + 1 arrives on the other barrier, and it reaches
+    // tile j + 2 only through S(j + 2), which the issuer starts after it has
+    // seen all four arrivals of tile j, so no phase mixes two tiles.
     for (int j = 0; j < nT; ++j) {
-      const int st = j % kStages;
       const uint32_t t_s = tmem + t_lane + kBN * (2 * m + (j & 1));
       if (!mbar_wait(&sm.s_full[m][j & 1], (j >> 1) & 1, abort, a.err)) {
         alive = false;
         break;
       }
       tc_fence_after();
-      // the stage's slot mask (the stage is not refilled before PV of this tile)
-      if (!mbar_wait(&sm.kv_full[st], (j / kStages) & 1, abort, a.err)) {
-        alive = false;
-        break;
-      }
-      const uint64_t bits = sm.mask[st];
+      const uint64_t bits = j < kMaxMaskTiles ? sm.tmask[j] : tile_mask<kDense>(a, sm.kept, t0 + j);
       const uint32_t t_p = tmem + t_lane + TmemCols<MT>::kP + (kBN / 2) * (2 * m + (j & 1));
       bool rescale = false;
       float alpha = 1.f;
@@ -698,12 +719,14 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
         PKV_TMEM_ST32(t_p, pk);
         tmem_wait_st();
       }
-      if (!wait_pv(j - 1)) {
-        alive = false;
-        break;
-      }
       if (__any_sync(0xffffffffu, rescale)) {
-        // O_m *= alpha for this row (alpha = 1 for rows that keep their max)
+        // O_m *= alpha for this row (alpha = 1 for rows that keep their max),
+        // once PV(j - 1) has completed
+        if (j > 0 && !mbar_wait(&sm.o_done[m], (j - 1) & 1, abort, a.err)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < kHeadDim; c += 16) {
           uint32_t o[16];
@@ -718,10 +741,11 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
       // S_m read, P_m written, O_m rescaled: PV(m, j) and QK(m, j + 2) may go
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full[m]);
+      if (lane == 0) mbar_arrive(&sm.p_full[m][j & 1]);
     }
     // ---- epilogue: O_m row (64 columns, one TMEM read) to the output or the split's partial
-    const bool have_o = alive && nT > 0 && wait_pv(nT - 1);
+    const bool have_o = alive && nT > 0 && mbar_wait(&sm.mma_done[m], 0, abort, a.err);
+    if (have_o) tc_fence_after();
     const bool write = alive && row < a.n_q && (have_o || nT == 0);
     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
     const long long ro = ((long long)split * a.n_q + row) * H + h;
@@ -789,7 +813,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
         alive = false;
         break;
       }
-      const uint64_t bits = sm.mask[st];
+      const uint64_t bits = j < kMaxMaskTiles ? sm.tmask[j] : tile_mask<kDense>(a, sm.kept, t0 + j);
       const uint32_t kbase = smem_u32(&sm.k[st][0]), vbase = smem_u32(&sm.v[st][0]);
       // S^T: this warp's 16 slots x 8 queries
       float sc[4] = {0.f, 0.f, 0.f, 0.f};

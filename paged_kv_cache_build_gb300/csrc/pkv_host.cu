@@ -828,7 +828,7 @@ static pkv_status attend_args(pkv_t h, Stream* st, const void* q, int n_q, int l
   a->tbl = table_args(h, *st, st->d_tbl_idx, st->d_tbl_len, nullptr, nullptr);
   a->n_entries = np;
   a->n_slots = (long long)(np - 1) * h->Ps + last;
-  a->n_tiles = ceil_div(a->n_slots, 64);
+  a->n_tiles = attend_tc_tiles(a->n_slots);
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)h->D);
   a->scale_log2 = scale * 1.4426950408889634f;
   a->num_splits = 1;
@@ -956,7 +956,7 @@ pkv_status pkv_attend_sampled(pkv_t h, const void* q, int n_q, int sid, int laye
   a.n_entries_all = np;
   a.n_entries = n_kept;
   a.n_slots = (long long)(n_kept - 1) * h->Ps + last_len;
-  a.n_tiles = ceil_div(a.n_slots, 64);
+  a.n_tiles = attend_tc_tiles(a.n_slots);
   a.num_splits = attend_num_splits(n_q, h->H, a.n_slots, h->num_sms);
   if (a.num_splits > 1) {
     if (pkv_status r = ensure_scratch(h, partial_bytes(a))) return r;
@@ -1017,7 +1017,7 @@ pkv_status pkv_attend_blocksparse(pkv_t h, const void* q, int n_q, int sid, int 
   a.n_entries_all = np;
   if (n_kept < np) a.n_slots = (long long)n_kept * h->Ps;
   a.n_entries = n_kept;
-  a.n_tiles = ceil_div(a.n_slots, 64);
+  a.n_tiles = attend_tc_tiles(a.n_slots);
   a.num_splits = attend_num_splits(n_q, h->H, a.n_slots, h->num_sms);
   if (a.num_splits > 1) {
     if (pkv_status r = ensure_scratch(h, partial_bytes(a))) return r;
@@ -1057,7 +1057,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Tensor map over a dense [rows][heads][64] bf16 tensor: box of 64 rows x 1
+// Tensor map over a dense [rows][heads][64] bf16 tensor: box of kTileSlots rows x 1
 // head x 64 elements, 128-byte swizzle (the tensor-core operand layout), zero
 // fill past the last row.
 static bool encode_kv_map(CUtensorMap* m, const void* base, int heads, long long rows) {
@@ -1065,7 +1065,7 @@ static bool encode_kv_map(CUtensorMap* m, const void* base, int heads, long long
   if (!enc) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)rows};
   const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)heads * kHeadDim * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1u, 64u};
+  const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1u, (cuuint32_t)kTileSlots};
   const cuuint32_t elem[3] = {1u, 1u, 1u};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
              elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1095,9 +1095,9 @@ pkv_status pkv_attend_frames(pkv_t h, const void* q, const void* k, const void* 
   a.out = static_cast<uint16_t*>(out);
   a.n_q = tokens;
   a.heads = h->H;
-  a.page_size = 64;                 // no pages; keeps the kernel's page arithmetic defined
+  a.page_size = kTileSlots;         // no pages; keeps the kernel's page arithmetic defined
   a.n_slots = tokens;
-  a.n_tiles = ceil_div(tokens, 64);
+  a.n_tiles = attend_tc_tiles(tokens);
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)h->D);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.num_splits = 1;

@@ -10,6 +10,7 @@
 namespace pkv {
 
 constexpr int kHeadDim = 64;        // bf16 elements per (slot, head) row: 128 bytes
+constexpr int kTileSlots = 64;      // KV slots per tile of the attention kernel
 constexpr int kChunksPerRow = 8;    // 16-byte chunks per row
 constexpr int kMaxBatch = 32;       // streams per batched append
 constexpr int kMaxChunks = 16;      // chunks visible at once (chunked mode)
@@ -152,6 +153,25 @@ struct TableArgs {
   int32_t* out_last;                // may be null
   int* err;
 };
+
+// Valid slots of entry e of a stream's visible table, from the table's counters
+// alone (no device memory is read): patch pages are full; special pages hold
+// sp_full_len slots, the last one sp_last_len; a chunk's pages are full but its last.
+__host__ __device__ __forceinline__ int table_len(const TableArgs& t, int e) {
+  if (t.mode == 0) {
+    if (e < t.n_scale + t.win_count) return t.page_size;
+    const int k = e - t.n_scale - t.win_count;
+    return (k == t.n_special - 1) ? t.sp_last_len : t.sp_full_len;
+  }
+  int c = 0, base = 0;
+  while (c < t.n_chunks - 1 && e >= base + t.chunk_npages[c]) {
+    base += t.chunk_npages[c];
+    ++c;
+  }
+  const int k = e - base;
+  const int n = t.chunk_len[c] - k * t.page_size;
+  return n < t.page_size ? n : t.page_size;
+}
 
 // Entry e of a stream's visible table (page id, valid slots): scale pages, window
 // pages oldest first, special pages (frame mode); chunks oldest first (chunked).

@@ -102,14 +102,14 @@ def test_noalloc_rejects_more_than_its_scratch(lib):
 
 
 def test_noalloc_chunked_uses_the_static_scratch(lib):
-    """A small chunked stream (chunks of 2 x 300 tokens, 4 visible, 4 heads,
+    """A small chunked stream (chunks of 2 x 400 tokens, 4 visible, 4 heads,
     64-slot pages) whose whole-chunk call fits the fixed array: every call runs in
     several KV splits (two launches: the attention and the combine that reads the
     partials back from the array) and matches pkv_attend_chunked, twice in a row."""
     from paged_kv_cache_build_gb300 import PagedKVCache, chunked_stream_cfg, kernel_launches
     w = WORKLOADS["chunked"]
-    heads, tokens, chunk, window = 4, 300, 2, 4
-    cache = PagedKVCache(64, 64, heads, 64)
+    heads, tokens, chunk, window = 4, 400, 2, 4
+    cache = PagedKVCache(128, 64, heads, 64)
     sid = cache.open_stream(chunked_stream_cfg(chunk, window, tokens))
     kv = torch.empty((2, chunk, tokens, heads, 64), dtype=torch.bfloat16, device="cuda")
     q = torch.empty((chunk * tokens, heads, 64), dtype=torch.bfloat16, device="cuda")
