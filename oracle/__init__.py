@@ -23,11 +23,14 @@ Sources (page title, section):
     (frame attention, each frame's tokens over that frame's own tokens,
     alternating with the global attention); section 5 (KV compression: the
     per-layer random page subset of sampling.py, and the page skipping by
-    estimated attention mass of blocksparse.py).
+    estimated attention mass of blocksparse.py); section 3.4, acceleration
+    dimension 5 (KV cache FP8: the E4M3 pages with power-of-two row scales of
+    fp8.py).
 
 Parity of every function here is pinned in tests/test_oracle_*.py against a
 brute-force flat model, closed forms, a library softmax-attention routine and
-a hand-derived page trace (tests/golden/).
+a hand-derived page trace (tests/golden/); fp8.py against the library's
+float8_e4m3fn type and the closed-form properties of its scale.
 """
 
 from .cache import OracleError, PagedCacheOracle, StreamConfig  # noqa: F401
