@@ -115,6 +115,27 @@ pkv_status pkv_create(int pool_pages, int page_size, int heads, int head_dim, pk
 pkv_status pkv_create_ex(int pool_pages, int page_size, int heads, int head_dim, int layers,
                          int max_streams, pkv_t* out);
 
+/* As pkv_create_ex, but the pages hold FP8 keys and values (vLLM-Omni RFC
+ * "Reconstruction Engine", section 3.4, acceleration dimension 5: KV cache FP8,
+ * about half the memory). Every stored row of head_dim = 64 values (one token,
+ * one head, K or V) is kept as 64 OCP E4M3 codes (1 sign, 4 exponent bits with
+ * bias 7, 3 mantissa bits; largest magnitude 448) of v * 2^-e and one exponent
+ * byte e: the smallest integer with max|v| <= 448 * 2^e (0 for a zero row),
+ * codes rounded to nearest, ties to even. So a row holds decode(code) * 2^e,
+ * which is exact in bf16, and the quantization is the format's only rounding.
+ * A page takes 2 * heads * page_size * 65 bytes instead of * 128. Append,
+ * rollback, eviction, the windowed reset and every attention call work as on
+ * bf16 pages; the attention dequantizes each K/V tile in shared memory and
+ * computes exactly what bf16 pages holding the dequantized values would give.
+ * K and V must be finite with magnitude below 2^126.
+ * Page layout (for callers that read the pool): per page the codes
+ * [kv][head][slot][64] bytes, unswizzled, then the exponents [kv][head][slot]
+ * as int8. pkv_attend_blocksparse and pkv_read_page refuse FP8 caches
+ * (pkv_read_page_fp8 reads them).
+ * Errors: as pkv_create_ex. */
+pkv_status pkv_create_fp8(int pool_pages, int page_size, int heads, int head_dim, int layers,
+                          int max_streams, pkv_t* out);
+
 /* Free everything. Synchronises the device first. NULL is accepted. Always OK. */
 pkv_status pkv_destroy(pkv_t h);
 
@@ -300,8 +321,8 @@ pkv_status pkv_attend_frames(pkv_t h, const void* q, const void* k, const void* 
  * keep >= 0 (at least the number of non-anchor pages keeps them all). The
  * estimate, the selection and the attention all run on the device (no host
  * round trip); the first call allocates a small device buffer.
- * Errors: as pkv_attend; STATE for a chunked-mode stream; INVALID for keep < 0 or
- * more than 1024 visible pages. */
+ * Errors: as pkv_attend; STATE for a chunked-mode stream; INVALID for keep < 0,
+ * more than 1024 visible pages, or an FP8 cache. */
 pkv_status pkv_attend_blocksparse(pkv_t h, const void* q, int n_q, int stream_id, int layer,
                                   void* out, float sm_scale, int keep, void* cuda_stream);
 
@@ -376,8 +397,15 @@ pkv_status pkv_export_state(pkv_t h, int stream_id, int32_t* host_buf, size_t ca
 
 /* Debug / test read of one page's K (kv = 0) or V (kv = 1) of one layer, copied to
  * host_dst as plain bf16 [heads][page_size][64] (un-swizzled). Synchronous.
- * Errors: INVALID (null pointer; layer, page or kv out of range), CUDA. */
+ * Errors: INVALID (null pointer; layer, page or kv out of range; an FP8 cache), CUDA. */
 pkv_status pkv_read_page(pkv_t h, int layer, int page, int kv, void* host_dst);
+
+/* Debug / test read of one page's K (kv = 0) or V (kv = 1) of one layer of an FP8
+ * cache (pkv_create_fp8), as stored: codes_dst receives uint8 [heads][page_size][64]
+ * E4M3 codes, exps_dst int8 [heads][page_size] row exponents; both are HOST
+ * buffers. Synchronous.
+ * Errors: INVALID (null pointer; layer, page or kv out of range; a bf16 cache), CUDA. */
+pkv_status pkv_read_page_fp8(pkv_t h, int layer, int page, int kv, void* codes_dst, void* exps_dst);
 
 /* Synthetic input generator (not part of the cache): fills dst, a device bf16
  * array [n_frames][n_tokens][heads][head_dim], with the counter-based ~N(0,1)

@@ -23,6 +23,7 @@ class StreamCfg(ctypes.Structure):
 SIGNATURES = {
     "pkv_create": (c_int, [c_int, c_int, c_int, c_int, ctypes.POINTER(c_void_p)]),
     "pkv_create_ex": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int, ctypes.POINTER(c_void_p)]),
+    "pkv_create_fp8": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int, ctypes.POINTER(c_void_p)]),
     "pkv_destroy": (c_int, [c_void_p]),
     "pkv_stream_open": (c_int, [c_void_p, ctypes.POINTER(StreamCfg), ctypes.POINTER(c_int)]),
     "pkv_stream_close": (c_int, [c_void_p, c_int, c_void_p]),
@@ -56,6 +57,7 @@ SIGNATURES = {
     "pkv_free_pages": (c_int, [c_void_p, ctypes.POINTER(c_int)]),
     "pkv_export_state": (c_int, [c_void_p, c_int, c_int32_p, c_size_t, ctypes.POINTER(c_size_t)]),
     "pkv_read_page": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p]),
+    "pkv_read_page_fp8": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
     "pkv_synth_fill": (c_int, [c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                c_int, c_int, c_int, c_float, c_void_p]),
     "pkv_kernel_launches": (ctypes.c_ulonglong, []),

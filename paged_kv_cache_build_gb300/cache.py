@@ -40,13 +40,15 @@ def chunked_stream_cfg(chunk_size, sliding_window_num, tokens_per_frame):
 class PagedKVCache:
     """A page pool (per layer) with its free list, shared by up to max_streams streams."""
 
-    def __init__(self, pool_pages, page_size, heads, head_dim=64, layers=1, max_streams=64):
+    def __init__(self, pool_pages, page_size, heads, head_dim=64, layers=1, max_streams=64,
+                 fp8=False):
         self.lib = load()
         self.pool_pages, self.page_size, self.heads, self.head_dim = pool_pages, page_size, heads, head_dim
         self.layers = layers
+        self.fp8 = bool(fp8)
         h = ctypes.c_void_p()
-        check(self.lib.pkv_create_ex(pool_pages, page_size, heads, head_dim, layers, max_streams,
-                                     ctypes.byref(h)), None)
+        create = self.lib.pkv_create_fp8 if fp8 else self.lib.pkv_create_ex
+        check(create(pool_pages, page_size, heads, head_dim, layers, max_streams, ctypes.byref(h)), None)
         self.h = h
 
     def close(self):
@@ -253,6 +255,17 @@ class PagedKVCache:
         idx = w[2 + f:2 + f + n]
         lens = w[2 + f + n:2 + f + 2 * n]
         return free, idx, lens, w[2 + f + 2 * n:]
+
+    def read_page_fp8(self, page, kv, layer=0):
+        """One page's K (kv=0) or V (kv=1) of an FP8 cache as stored: (codes uint8
+        [heads][page_size][64], exponents int8 [heads][page_size])."""
+        import numpy as np
+        codes = np.empty((self.heads, self.page_size, self.head_dim), dtype=np.uint8)
+        exps = np.empty((self.heads, self.page_size), dtype=np.int8)
+        self._check(self.lib.pkv_read_page_fp8(self.h, layer, page, kv,
+                                               codes.ctypes.data_as(ctypes.c_void_p),
+                                               exps.ctypes.data_as(ctypes.c_void_p)))
+        return codes, exps
 
     def read_page(self, page, kv, layer=0):
         """One page's K (kv=0) or V (kv=1) as a host uint16 array [heads][page_size][64]."""

@@ -41,6 +41,7 @@
 // error word, and the CTA drains its copies and MMAs and frees TMEM before
 // returning.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <atomic>
 #include <type_traits>
@@ -70,7 +71,26 @@ constexpr uint32_t kSpinLimit = 1u << 25;
 // 2^(s - m) exceeds 2^64 (or overflows), the row's reference moves to its max.
 constexpr float kSumLimit = 18446744073709551616.0f;   // 2^64
 
-template <int MT>
+// FP8 pages: the producer bulk-copies a tile's E4M3 codes and row exponents into
+// a staging ring; two warps dequantize them into the bf16 operand ring.
+constexpr int kF8Stages = 4;
+template <bool FP8>
+struct __align__(128) F8Ring {
+  alignas(128) uint8_t k[kF8Stages][kBN * kHeadDim];   // codes, 64-byte rows (unswizzled)
+  alignas(128) uint8_t v[kF8Stages][kBN * kHeadDim];
+  alignas(128) int8_t ke[kF8Stages][kBN];               // row exponents
+  alignas(128) int8_t ve[kF8Stages][kBN];
+  int nblk[kF8Stages];                     // page blocks copied into the stage
+  uint64_t full[kF8Stages];                // the stage's copies have landed
+  uint64_t free_[kF8Stages];               // both converting warps are done with it
+};
+template <>
+struct F8Ring<false> {
+  uint64_t unused;
+};
+static_assert(sizeof(F8Ring<true>) % 128 == 0, "staging ring alignment");
+
+template <int MT, bool FP8 = false>
 struct __align__(1024) TcSmem {
   uint8_t q[MT][128 * 128];          // Q_m: 128 rows x 64 bf16, 128B-swizzled
   uint8_t k[kStages][kBN * 128];     // K tile: 64 slots x 64 bf16
@@ -86,9 +106,11 @@ struct __align__(1024) TcSmem {
   uint64_t o_done[MT];               // PV of the latest tile has completed (waited only to rescale O)
   uint64_t mma_done[MT];
   uint64_t x_done;                   // the extra-row warps have published their partials
+  F8Ring<FP8> f8;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(TcSmem<2, true>) + 1024 <= 232448, "shared memory of the largest variant");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -303,10 +325,15 @@ __device__ __forceinline__ uint32_t sw_addr(uint32_t base, int r, int c) {
 }
 
 // Warps: 0 extra rows, 1 MMA issuer (M-tile 1), 2 producer, 3 MMA issuer
-// (M-tile 0), 4 .. 4 + 4 MT - 1 softmax, then kXWarps - 1 more extra-row warps.
-template <int MT, bool EXTRA>
+// (M-tile 0), 4 .. 4 + 4 MT - 1 softmax, then kXWarps - 1 more extra-row warps,
+// then (FP8 pages) the second dequantizing warp.
+template <int MT, bool EXTRA, bool FP8 = false>
 __host__ __device__ constexpr int tc_threads() {
-  return (4 + 4 * MT + (EXTRA ? kXWarps - 1 : 0)) * 32;
+  return (4 + 4 * MT + (EXTRA ? kXWarps - 1 : 0) + (FP8 ? 1 : 0)) * 32;
+}
+template <int MT, bool EXTRA>
+__host__ __device__ constexpr int tc_conv_warp() {
+  return 4 + 4 * MT + (EXTRA ? kXWarps - 1 : 0);
 }
 constexpr int kXWarp = 0;
 constexpr int kProducerWarp = 2;
@@ -358,11 +385,49 @@ __device__ __forceinline__ uint64_t tile_mask(const AttendArgs& a, const uint16_
   return bits;
 }
 
-template <int MT, bool EXTRA, typename Params>
-__global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
+// Dequantizes `rows` 64-value rows of FP8 codes (with their exponents) from a
+// staging stage into a bf16 operand tile at its 128-byte-swizzled place, two rows
+// per lane of one warp (row base + lane, base + 32 + lane). decode(code) is exact
+// in f16, f16 -> fp32 is exact, and the power-of-two scale and the final bf16
+// rounding are exact for these values (at most 4 significant bits).
+__device__ __forceinline__ void fp8_dequant_rows(const uint8_t* codes, const int8_t* exps,
+                                                 uint8_t* dst, int rows, int lane) {
+  for (int r = lane; r < rows; r += 32) {
+    const int e = exps[r];
+    // 2^e as two normal fp32 factors (e may be -127)
+    const float s1 = __uint_as_float((uint32_t)(127 + (e >> 1)) << 23);
+    const float s2 = __uint_as_float((uint32_t)(127 + e - (e >> 1)) << 23);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 in = *reinterpret_cast<const uint4*>(codes + r * kHeadDim + 16 * q);
+      const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+      uint32_t out[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int hw = 0; hw < 2; ++hw) {
+          const uint16_t pair = (uint16_t)(w[i] >> (16 * hw));
+          uint32_t h2;
+          asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(h2) : "h"(pair));
+          const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * s1 * s2;
+          const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16))) * s1 * s2;
+          out[2 * i + hw] = pack_bf16(lo, hi);
+        }
+      }
+      uint8_t* row = dst + r * 128;
+      *reinterpret_cast<uint4*>(row + (swizzle_chunk(r, 2 * q) << 4)) =
+          make_uint4(out[0], out[1], out[2], out[3]);
+      *reinterpret_cast<uint4*>(row + (swizzle_chunk(r, 2 * q + 1) << 4)) =
+          make_uint4(out[4], out[5], out[6], out[7]);
+    }
+  }
+}
+
+template <int MT, bool EXTRA, bool FP8, typename Params>
+__global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
     attend_tc_kernel(const __grid_constant__ Params params, int n_mgroups_1, int n_tiles_1) {
   extern __shared__ uint8_t smem_raw[];
-  TcSmem<MT>& sm = *reinterpret_cast<TcSmem<MT>*>(
+  TcSmem<MT, FP8>& sm = *reinterpret_cast<TcSmem<MT, FP8>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const CtaWork cw = cta_work(params, n_mgroups_1, n_tiles_1);
@@ -388,8 +453,14 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   // ---- set-up: barriers, zeroed KV ring, Q tiles, TMEM
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv_full[s], FP8 ? 2 : 1);          // copy (tx) or the two dequantizers
       mbar_init(&sm.kv_empty[s], MT + (EXTRA ? kXWarps : 0));   // MMA issuers, extra warps
+    }
+    if constexpr (FP8) {
+      for (int s = 0; s < kF8Stages; ++s) {
+        mbar_init(&sm.f8.full[s], 1);
+        mbar_init(&sm.f8.free_[s], 2);
+      }
     }
     for (int m = 0; m < MT; ++m) {
       mbar_init(&sm.s_full[m][0], 1);
@@ -426,7 +497,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   if (warp != kProducerWarp) {
     // Q tiles: every load issued before the first store; the producer warp
     // meanwhile starts on the KV ring
-    constexpr int kThreads = tc_threads<MT, EXTRA>() - 32;
+    constexpr int kThreads = tc_threads<MT, EXTRA, FP8>() - 32;
     constexpr int kQ = MT * 128 * 8;               // 16-byte chunks
     constexpr int kQPer = (kQ + kThreads - 1) / kThreads;
     const int qt = warp < kProducerWarp ? (int)threadIdx.x : (int)threadIdx.x - 32;
@@ -476,7 +547,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   // (the softmax and extra-row warps), so that the tile loops read neither the
   // kernel's parameters nor the stage's copy barrier for them.
   if (warp != kProducerWarp) {
-    constexpr int kThreads = tc_threads<MT, EXTRA>() - 32;
+    constexpr int kThreads = tc_threads<MT, EXTRA, FP8>() - 32;
     const int tt = warp < kProducerWarp ? (int)threadIdx.x : (int)threadIdx.x - 32;
     for (int j = tt; j < nT && j < kMaxMaskTiles; j += kThreads)
       sm.tmask[j] = tile_mask<kDense>(a, sm.kept, t0 + j);
@@ -493,7 +564,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   // needs neither (named barrier 1: all warps but the producer)
   if (warp != kProducerWarp) {
     tc_fence_before();
-    asm volatile("bar.sync 1, %0;\n" ::"r"(tc_threads<MT, EXTRA>() - 32) : "memory");
+    asm volatile("bar.sync 1, %0;\n" ::"r"(tc_threads<MT, EXTRA, FP8>() - 32) : "memory");
     tc_fence_after();
   }
   const uint32_t tmem = sm.tmem_base;
@@ -525,7 +596,89 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     }
     const int per = Ps >= kBN ? 1 : kBN / Ps;      // page blocks per tile
     const int rows = Ps >= kBN ? kBN : Ps;         // slots per block
-    for (int j = 0; !kDense && j < nT; ++j) {
+    if constexpr (FP8 && !kDense) {
+      // FP8 pages: each tile's codes and row exponents are copied into a staging
+      // stage kF8Stages tiles ahead; this warp dequantizes the K rows into the
+      // operand ring (the second converting warp the V rows) and refills the
+      // stage once both are done with it
+      auto issue_stage = [&](int j) {
+        const int st8 = j % kF8Stages;
+        const int tile = t0 + j;
+        int nblk = 0, blk_page[kBN / 16], blk_so[kBN / 16];
+#pragma unroll
+        for (int pp = 0; pp < kBN / 16; ++pp) {
+          if (pp >= per) break;
+          const int f0 = tile * kBN + pp * rows;
+          const int e = f0 / Ps, so = f0 - e * Ps;
+          if (e >= a.n_entries) break;
+          if ((e & ~31) != e_batch) {              // warp-uniform: next batch of entries
+            e_batch = e & ~31;
+            e_page = e_len = 0;
+            if (e_batch + lane < a.n_entries) table_entry(a.tbl, entry_of(e_batch + lane), e_page, e_len);
+          }
+          blk_page[pp] = __shfl_sync(0xffffffffu, e_page, e - e_batch);
+          blk_so[pp] = so;
+          nblk = pp + 1;
+        }
+        if (lane == 0) {
+          sm.f8.nblk[st8] = nblk;
+          const uint32_t mb = smem_u32(&sm.f8.full[st8]);
+          mbar_arrive_expect_tx(&sm.f8.full[st8], (uint32_t)nblk * 2u * rows * (kHeadDim + 1));
+#pragma unroll
+          for (int pp = 0; pp < kBN / 16; ++pp) {
+            if (pp >= nblk) break;
+            int page = blk_page[pp];
+            if (page < 0 || page >= a.pool_pages) {
+              atomicOr(a.err, kErrPageRange);
+              page = 0;
+            }
+            const uint8_t* pg = reinterpret_cast<const uint8_t*>(a.pool) + (long long)page * a.page_bytes;
+            const long long rk = (long long)h * Ps + blk_so[pp];          // K row of the block
+            const long long rv = (long long)(H + h) * Ps + blk_so[pp];    // V row
+            const uint32_t code_bytes = (uint32_t)rows * kHeadDim;
+            const uint32_t dsts[4] = {smem_u32(&sm.f8.k[st8][pp * rows * kHeadDim]),
+                                      smem_u32(&sm.f8.v[st8][pp * rows * kHeadDim]),
+                                      smem_u32(&sm.f8.ke[st8][pp * rows]),
+                                      smem_u32(&sm.f8.ve[st8][pp * rows])};
+            const uint8_t* srcs[4] = {pg + rk * kHeadDim, pg + rv * kHeadDim, pg + a.exp_off + rk,
+                                      pg + a.exp_off + rv};
+            const uint32_t sizes[4] = {code_bytes, code_bytes, (uint32_t)rows, (uint32_t)rows};
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              asm volatile(
+                  "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
+                  "%2, [%3];\n" ::"r"(dsts[c]),
+                  "l"(srcs[c]), "r"(sizes[c]), "r"(mb)
+                  : "memory");
+          }
+        }
+      };
+      int issued = 0, consumed = 0;
+      for (; issued < nT && issued < kF8Stages; ++issued) issue_stage(issued);
+      for (int j = 0; j < nT; ++j) {
+        const int st8 = j % kF8Stages, s = j % kStages;
+        if (!mbar_wait(&sm.f8.full[st8], (j / kF8Stages) & 1, abort, a.err)) break;
+        consumed = j + 1;
+        if (!mbar_wait(&sm.kv_empty[s], ((j / kStages) & 1) ^ 1, abort, a.err)) break;
+        fp8_dequant_rows(sm.f8.k[st8], sm.f8.ke[st8], sm.k[s], sm.f8.nblk[st8] * rows, lane);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sm.kv_full[s]);
+          mbar_arrive(&sm.f8.free_[st8]);
+        }
+        if (issued < nT) {
+          if (!mbar_wait(&sm.f8.free_[st8], (j / kF8Stages) & 1, abort, a.err)) break;
+          issue_stage(issued);
+          ++issued;
+        }
+      }
+      // no copy may still be landing in shared memory when the CTA ends
+      if (lane == 0)
+        for (int j = consumed; j < issued; ++j)
+          mbar_wait(&sm.f8.full[j % kF8Stages], (j / kF8Stages) & 1, abort, a.err, false);
+    }
+    for (int j = 0; !kDense && !FP8 && j < nT; ++j) {
       const int s = j % kStages;
       if (!mbar_wait(&sm.kv_empty[s], ((j / kStages) & 1) ^ 1, abort, a.err)) break;
       const int tile = t0 + j;
@@ -788,7 +941,24 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
     }
     if (write && a.num_splits > 1)
       *reinterpret_cast<float2*>(a.part_ml + ro * 2) = make_float2(m_run, l_run);
-  } else if (EXTRA && (warp == kXWarp || warp >= 4 + 4 * MT)) {
+  } else if (FP8 && !kDense && warp == tc_conv_warp<MT, EXTRA>()) {
+    // ===================================================== V dequantizer (FP8)
+    if constexpr (FP8 && !kDense) {
+      const int rows = Ps >= kBN ? kBN : Ps;
+      for (int j = 0; j < nT; ++j) {
+        const int st8 = j % kF8Stages, s = j % kStages;
+        if (!mbar_wait(&sm.f8.full[st8], (j / kF8Stages) & 1, abort, a.err)) break;
+        if (!mbar_wait(&sm.kv_empty[s], ((j / kStages) & 1) ^ 1, abort, a.err)) break;
+        fp8_dequant_rows(sm.f8.v[st8], sm.f8.ve[st8], sm.v[s], sm.f8.nblk[st8] * rows, lane);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sm.kv_full[s]);
+          mbar_arrive(&sm.f8.free_[st8]);
+        }
+      }
+    }
+  } else if (EXTRA && (warp == kXWarp || (warp >= 4 + 4 * MT && warp < tc_conv_warp<MT, EXTRA>()))) {
     // ============================================== extra rows (mma.sync, regs)
     // Up to 8 query rows, shared by kXWarps warps: warp xi takes slots 16 xi ..
     // 16 xi + 15 of every tile with its own running max, sum and O, and the
@@ -952,9 +1122,9 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA>(), 1)
   }
 }
 
-template <int MT, bool EXTRA, typename Params>
+template <int MT, bool EXTRA, bool FP8, typename Params>
 cudaError_t launch_mt(const Params& p, int grid, int n_mgroups, int n_tiles, cudaStream_t s) {
-  const size_t smem = sizeof(TcSmem<MT>) + 1024;
+  const size_t smem = sizeof(TcSmem<MT, FP8>) + 1024;
   // the shared-memory opt-in is a per-device function attribute: set it once for
   // every device this process launches on
   static std::atomic<unsigned long long> configured{0};
@@ -962,13 +1132,13 @@ cudaError_t launch_mt(const Params& p, int grid, int n_mgroups, int n_tiles, cud
   if (cudaError_t e = cudaGetDevice(&dev)) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (dev >= 64 || !(configured.load() & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<MT, EXTRA, Params>,
+    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<MT, EXTRA, FP8, Params>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (dev < 64) configured.fetch_or(bit);
   }
-  const cudaError_t e = launch_pdl(attend_tc_kernel<MT, EXTRA, Params>, dim3(grid),
-                                   dim3(tc_threads<MT, EXTRA>()), smem, s, p, n_mgroups, n_tiles);
+  const cudaError_t e = launch_pdl(attend_tc_kernel<MT, EXTRA, FP8, Params>, dim3(grid),
+                                   dim3(tc_threads<MT, EXTRA, FP8>()), smem, s, p, n_mgroups, n_tiles);
   count_launches(1);
   return e;
 }
@@ -1023,32 +1193,37 @@ int attend_tc_splits_pairs(int pairs, int n_tiles, int num_sms) {
   return best;
 }
 
-template <typename Params>
+template <bool FP8, typename Params>
 static cudaError_t launch_shape(int shape, const Params& p, int grid, int n_mgroups, int n_tiles,
                                 cudaStream_t s) {
   switch (shape) {
-    case 0: return launch_mt<1, false>(p, grid, n_mgroups, n_tiles, s);
-    case 1: return launch_mt<1, true>(p, grid, n_mgroups, n_tiles, s);
-    case 2: return launch_mt<2, false>(p, grid, n_mgroups, n_tiles, s);
-    default: return launch_mt<2, true>(p, grid, n_mgroups, n_tiles, s);
+    case 0: return launch_mt<1, false, FP8>(p, grid, n_mgroups, n_tiles, s);
+    case 1: return launch_mt<1, true, FP8>(p, grid, n_mgroups, n_tiles, s);
+    case 2: return launch_mt<2, false, FP8>(p, grid, n_mgroups, n_tiles, s);
+    default: return launch_mt<2, true, FP8>(p, grid, n_mgroups, n_tiles, s);
   }
 }
 
 cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t s) {
   const TcShape sh = tc_shape(a.n_q);
   const int n_tiles = attend_tc_tiles(a.n_slots);
-  return launch_shape(attend_tc_shape(a.n_q), a, sh.n_mgroups * a.heads * a.num_splits,
-                      sh.n_mgroups, n_tiles, s);
+  if (a.fp8)
+    return launch_shape<true>(attend_tc_shape(a.n_q), a, sh.n_mgroups * a.heads * a.num_splits,
+                              sh.n_mgroups, n_tiles, s);
+  return launch_shape<false>(attend_tc_shape(a.n_q), a, sh.n_mgroups * a.heads * a.num_splits,
+                             sh.n_mgroups, n_tiles, s);
 }
 
 cudaError_t launch_attend_tc_batch(const AttendBatch& b, cudaStream_t s) {
-  return launch_shape(attend_tc_shape(b.item[0].n_q), b, b.cta_base[b.n], 0, 0, s);
+  if (b.item[0].fp8)
+    return launch_shape<true>(attend_tc_shape(b.item[0].n_q), b, b.cta_base[b.n], 0, 0, s);
+  return launch_shape<false>(attend_tc_shape(b.item[0].n_q), b, b.cta_base[b.n], 0, 0, s);
 }
 
 cudaError_t launch_attend_dense(const AttendDense& d, int n_frames, cudaStream_t s) {
   const TcShape sh = tc_shape(d.a.n_q);
-  return launch_shape(attend_tc_shape(d.a.n_q), d, sh.n_mgroups * d.a.heads * n_frames,
-                      sh.n_mgroups, d.a.n_tiles, s);
+  return launch_shape<false>(attend_tc_shape(d.a.n_q), d, sh.n_mgroups * d.a.heads * n_frames,
+                             sh.n_mgroups, d.a.n_tiles, s);
 }
 
 }  // namespace pkv

@@ -58,7 +58,10 @@ struct Stream {
 
 struct pkv_ctx {
   int P = 0, Ps = 0, H = 0, D = 0, L = 0, max_streams = 0;
-  long long page_elems = 0;
+  long long page_elems = 0;      // bf16 elements per page (bf16 pools)
+  int fp8 = 0;                   // 1: E4M3 pages with row exponents
+  long long page_bytes = 0;      // bytes per page (either format)
+  long long exp_off = 0;         // FP8 pages: byte offset of the row exponents
   uint16_t* d_pool = nullptr;
   int32_t* d_free = nullptr;
   int* d_err = nullptr;
@@ -108,13 +111,22 @@ pkv_status cuda_fail(pkv_t h, cudaError_t e, const char* what) {
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Layer `layer`'s page set (a byte offset, so that it holds for either format).
+inline uint16_t* layer_base(pkv_t h, int layer) {
+  return reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(h->d_pool) +
+                                     (long long)layer * h->P * h->page_bytes);
+}
+
 inline PoolView pool_view(pkv_t h, int layer) {
   PoolView pv;
-  pv.base = h->d_pool + (long long)layer * h->P * h->page_elems;
+  pv.base = layer_base(h, layer);
   pv.page_elems = h->page_elems;
   pv.heads = h->H;
   pv.page_size = h->Ps;
   pv.pool_pages = h->P;
+  pv.fp8 = h->fp8;
+  pv.page_bytes = h->page_bytes;
+  pv.exp_off = h->exp_off;
   return pv;
 }
 
@@ -241,8 +253,10 @@ pkv_status pkv_create(int pool_pages, int page_size, int heads, int head_dim, pk
   return pkv_create_ex(pool_pages, page_size, heads, head_dim, 1, 64, out);
 }
 
-pkv_status pkv_create_ex(int pool_pages, int page_size, int heads, int head_dim, int layers,
-                         int max_streams, pkv_t* out) {
+}  // extern "C"
+
+static pkv_status create_cache(int pool_pages, int page_size, int heads, int head_dim, int layers,
+                               int max_streams, int fp8, pkv_t* out) {
   if (!out) return fail(nullptr, PKV_ERR_INVALID, "null output handle");
   *out = nullptr;
   if (head_dim != kHeadDim) return fail(nullptr, PKV_ERR_INVALID, "head_dim must be 64");
@@ -261,6 +275,10 @@ pkv_status pkv_create_ex(int pool_pages, int page_size, int heads, int head_dim,
   h->L = layers;
   h->max_streams = max_streams;
   h->page_elems = 2LL * heads * page_size * head_dim;
+  h->fp8 = fp8;
+  // FP8 pages: 64 code bytes and one exponent byte per row; bf16 pages: 128 bytes per row
+  h->page_bytes = fp8 ? 2LL * heads * page_size * (head_dim + 1) : 2LL * h->page_elems;
+  h->exp_off = fp8 ? 2LL * heads * page_size * head_dim : 0;
   h->streams.resize(max_streams);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -272,7 +290,7 @@ pkv_status pkv_create_ex(int pool_pages, int page_size, int heads, int head_dim,
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     h->noalloc_scratch = static_cast<float*>(p);
   }
-  const size_t pool_bytes = (size_t)layers * pool_pages * h->page_elems * sizeof(uint16_t);
+  const size_t pool_bytes = (size_t)layers * pool_pages * h->page_bytes;
   if (e == cudaSuccess) e = cudaMalloc(&h->d_pool, pool_bytes);
   if (e == cudaSuccess) e = cudaMemset(h->d_pool, 0, pool_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&h->d_free, sizeof(int32_t) * pool_pages);
@@ -293,6 +311,18 @@ pkv_status pkv_create_ex(int pool_pages, int page_size, int heads, int head_dim,
   h->free_top = pool_pages;
   *out = h;
   return PKV_OK;
+}
+
+extern "C" {
+
+pkv_status pkv_create_ex(int pool_pages, int page_size, int heads, int head_dim, int layers,
+                         int max_streams, pkv_t* out) {
+  return create_cache(pool_pages, page_size, heads, head_dim, layers, max_streams, 0, out);
+}
+
+pkv_status pkv_create_fp8(int pool_pages, int page_size, int heads, int head_dim, int layers,
+                          int max_streams, pkv_t* out) {
+  return create_cache(pool_pages, page_size, heads, head_dim, layers, max_streams, 1, out);
 }
 
 pkv_status pkv_destroy(pkv_t h) {
@@ -701,6 +731,10 @@ static pkv_status window_reset(pkv_t h, Stream* st, cudaStream_t s) {
   ca.pool = h->d_pool;
   ca.layer_elems = (long long)h->P * h->page_elems;
   ca.page_elems = h->page_elems;
+  ca.fp8 = h->fp8;
+  ca.layer_bytes = (long long)h->P * h->page_bytes;
+  ca.page_bytes = h->page_bytes;
+  ca.exp_off = h->exp_off;
   ca.layers = h->L;
   ca.heads = h->H;
   ca.page_size = h->Ps;
@@ -821,8 +855,11 @@ static pkv_status attend_args(pkv_t h, Stream* st, const void* q, int n_q, int l
   a->out = static_cast<uint16_t*>(out);
   a->n_q = n_q;
   a->heads = h->H;
-  a->pool = h->d_pool + (long long)layer * h->P * h->page_elems;
+  a->pool = layer_base(h, layer);
   a->page_elems = h->page_elems;
+  a->page_bytes = h->page_bytes;
+  a->exp_off = h->exp_off;
+  a->fp8 = h->fp8;
   a->page_size = h->Ps;
   a->pool_pages = h->P;
   a->tbl = table_args(h, *st, st->d_tbl_idx, st->d_tbl_len, nullptr, nullptr);
@@ -973,6 +1010,7 @@ pkv_status pkv_attend_blocksparse(pkv_t h, const void* q, int n_q, int sid, int 
   if (st->cfg.mode != PKV_MODE_FRAME)
     return fail(h, PKV_ERR_STATE, "pkv_attend_blocksparse needs a frame-mode stream");
   if (keep < 0) return fail(h, PKV_ERR_INVALID, "keep %d < 0", keep);
+  if (h->fp8) return fail(h, PKV_ERR_INVALID, "page skipping by mass reads bf16 pages; this cache holds FP8 pages");
   AttendArgs a;
   if (pkv_status r = attend_args(h, st, q, n_q, layer, out, sm_scale, &a)) return r;
   const int np = a.n_entries;
@@ -1253,11 +1291,11 @@ pkv_status pkv_read_page(pkv_t h, int layer, int page, int kv, void* host_dst) {
   if (!h || !host_dst) return fail(h, PKV_ERR_INVALID, "null argument");
   if (layer < 0 || layer >= h->L || page < 0 || page >= h->P || (kv != 0 && kv != 1))
     return fail(h, PKV_ERR_INVALID, "layer/page/kv out of range");
+  if (h->fp8) return fail(h, PKV_ERR_INVALID, "this cache holds FP8 pages: use pkv_read_page_fp8");
   const size_t n = (size_t)h->H * h->Ps * kHeadDim;
   std::vector<uint16_t> raw(n);
   PKV_CUDA(h, cudaDeviceSynchronize());
-  const uint16_t* src = h->d_pool + (long long)layer * h->P * h->page_elems +
-                        (long long)page * h->page_elems + (long long)kv * n;
+  const uint16_t* src = layer_base(h, layer) + (long long)page * h->page_elems + (long long)kv * n;
   PKV_CUDA(h, cudaMemcpy(raw.data(), src, n * sizeof(uint16_t), cudaMemcpyDeviceToHost));
   uint16_t* dst = static_cast<uint16_t*>(host_dst);
   for (int hh = 0; hh < h->H; ++hh)
@@ -1266,6 +1304,21 @@ pkv_status pkv_read_page(pkv_t h, int layer, int page, int kv, void* host_dst) {
         const size_t row = ((size_t)hh * h->Ps + s) * kHeadDim;
         std::memcpy(dst + row + c * 8, raw.data() + row + swizzle_chunk(s, c) * 8, 16);
       }
+  return PKV_OK;
+}
+
+pkv_status pkv_read_page_fp8(pkv_t h, int layer, int page, int kv, void* codes_dst,
+                             void* exps_dst) {
+  if (!h || !codes_dst || !exps_dst) return fail(h, PKV_ERR_INVALID, "null argument");
+  if (layer < 0 || layer >= h->L || page < 0 || page >= h->P || (kv != 0 && kv != 1))
+    return fail(h, PKV_ERR_INVALID, "layer/page/kv out of range");
+  if (!h->fp8) return fail(h, PKV_ERR_INVALID, "this cache holds bf16 pages: use pkv_read_page");
+  const size_t rows = (size_t)h->H * h->Ps;
+  PKV_CUDA(h, cudaDeviceSynchronize());
+  const uint8_t* pg = reinterpret_cast<const uint8_t*>(layer_base(h, layer)) + (long long)page * h->page_bytes;
+  PKV_CUDA(h, cudaMemcpy(codes_dst, pg + (size_t)kv * rows * kHeadDim, rows * kHeadDim,
+                         cudaMemcpyDeviceToHost));
+  PKV_CUDA(h, cudaMemcpy(exps_dst, pg + h->exp_off + (size_t)kv * rows, rows, cudaMemcpyDeviceToHost));
   return PKV_OK;
 }
 

@@ -28,14 +28,88 @@ __host__ __device__ __forceinline__ int swizzle_chunk(int slot, int chunk) {
   return chunk ^ (slot & 7);
 }
 
-// One layer's page set: pool[page][kv][head][slot][64].
+// One layer's page set. bf16 pages: pool[page][kv][head][slot][64] bf16, rows
+// 128-byte swizzled. FP8 pages: per page the E4M3 codes [kv][head][slot][64]
+// (64-byte rows, unswizzled), then one exponent byte per row [kv][head][slot]
+// at exp_off: a row's values are decode(code) * 2^exponent.
 struct PoolView {
   uint16_t* base;
-  long long page_elems;   // 2 * heads * page_size * 64
+  long long page_elems;   // bf16 pages: 2 * heads * page_size * 64
   int heads;
   int page_size;
   int pool_pages;
+  int fp8;                // 1: E4M3 pages
+  long long page_bytes;   // bytes per page (either format)
+  long long exp_off;      // FP8 pages: byte offset of the exponents in a page
 };
+
+// ------------------------------------------------------------- FP8 rows
+// vLLM-Omni RFC "Reconstruction Engine", section 3.4 (quantization: KV cache
+// FP8). A row of 64 values is stored as OCP E4M3 codes of v * 2^-e with one
+// exponent e per row: the smallest integer with amax <= 448 * 2^e (amax the
+// row's largest magnitude; 0 for a zero row). With amax = f * 2^k, f in
+// [0.5, 1), and 448 = 0.875 * 2^9, e = k - 9 + (f > 0.875). bf16 inputs give e
+// in [-127, 120], so 2^-e is a normal fp32 value and v * 2^-e is exact.
+__device__ __forceinline__ int fp8_row_exponent(float amax) {
+  if (!(amax > 0.f)) return 0;
+  int k;
+  const float f = frexpf(amax, &k);
+  const int e = k - 9 + (f > 0.875f ? 1 : 0);
+  return e < -127 ? -127 : (e > 126 ? 126 : e);
+}
+
+// Two floats to two E4M3 codes, round to nearest even (a in the low byte).
+__device__ __forceinline__ uint32_t fp8_pack2(float a, float b) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+__device__ __forceinline__ uint8_t* fp8_row_codes(const PoolView& pv, int page, int kv, int head,
+                                                  int slot) {
+  return reinterpret_cast<uint8_t*>(pv.base) + (long long)page * pv.page_bytes +
+         ((long long)(kv * pv.heads + head) * pv.page_size + slot) * kHeadDim;
+}
+__device__ __forceinline__ int8_t* fp8_row_exp(const PoolView& pv, int page, int kv, int head,
+                                               int slot) {
+  return reinterpret_cast<int8_t*>(pv.base) + (long long)page * pv.page_bytes + pv.exp_off +
+         (long long)(kv * pv.heads + head) * pv.page_size + slot;
+}
+
+// Stores 16-byte chunk c (values 8c .. 8c + 7) of row (page, kv, head, slot).
+// bf16 pages: at its swizzled place. FP8 pages: the eight lanes that hold a
+// row's eight chunks (lanes 8g .. 8g + 7 of a warp, chunk = lane % 8) call this
+// together; they share the row's largest magnitude and write their 8 codes, and
+// chunk 0 writes the exponent.
+__device__ __forceinline__ void store_row_chunk(const PoolView& pv, int page, int kv, int head,
+                                                int slot, int c, const uint4& val) {
+  if (!pv.fp8) {
+    uint16_t* row = pv.base + (long long)page * pv.page_elems +
+                    ((long long)(kv * pv.heads + head) * pv.page_size + slot) * kHeadDim;
+    *reinterpret_cast<uint4*>(row + swizzle_chunk(slot, c) * 8) = val;
+    return;
+  }
+  const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+  float f[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  const unsigned group = 0xFFu << (threadIdx.x & 24);
+  amax = fmaxf(amax, __shfl_xor_sync(group, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(group, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(group, amax, 4));
+  const int e = fp8_row_exponent(amax);
+  const float inv = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e
+  const uint32_t lo = fp8_pack2(f[0] * inv, f[1] * inv) | (fp8_pack2(f[2] * inv, f[3] * inv) << 16);
+  const uint32_t hi = fp8_pack2(f[4] * inv, f[5] * inv) | (fp8_pack2(f[6] * inv, f[7] * inv) << 16);
+  *reinterpret_cast<uint2*>(fp8_row_codes(pv, page, kv, head, slot) + 8 * c) = make_uint2(lo, hi);
+  if (c == 0) *fp8_row_exp(pv, page, kv, head, slot) = (int8_t)e;
+}
 
 // ------------------------------------------------------------------ append
 struct AppendItem {                 // one frame-mode stream of a batched append
@@ -99,6 +173,8 @@ struct ResetCopyArgs {              // copy carried frames' special tokens, all 
   uint16_t* pool;                   // layer 0 base
   long long layer_elems;            // pool_pages * page_elems
   long long page_elems;
+  int fp8;                          // E4M3 pages: rows are codes + an exponent byte
+  long long layer_bytes, page_bytes, exp_off;
   int layers, heads, page_size, pool_pages;
   int n_special, f_sp;
   const int32_t* special_list;      // old special list
@@ -208,6 +284,9 @@ struct AttendArgs {
   int heads;
   const uint16_t* pool;             // layer base
   long long page_elems;
+  long long page_bytes;             // FP8 pages: bytes per page, and the exponents'
+  long long exp_off;                // byte offset inside a page
+  int fp8;                          // 1: the pool holds E4M3 pages
   int page_size;
   int pool_pages;
   TableArgs tbl;                     // the visible table, computed on the fly by the producer

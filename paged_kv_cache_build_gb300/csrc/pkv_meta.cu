@@ -24,12 +24,6 @@ __device__ __forceinline__ bool page_ok(int p, int pool_pages) {
   return p >= 0 && p < pool_pages;
 }
 
-__device__ __forceinline__ uint16_t* row_ptr(const PoolView& pv, int page, int kv, int head,
-                                             int slot) {
-  return pv.base + (long long)page * pv.page_elems +
-         ((long long)(kv * pv.heads + head) * pv.page_size + slot) * kHeadDim;
-}
-
 // Tokens moved by one append block (TPB): with several, each thread issues all
 // its loads before its stores and the block's set-up (page-need scan, barrier)
 // is shared; a single frame keeps one token per block so that it still spreads
@@ -109,16 +103,14 @@ __global__ void __launch_bounds__(512) frame_append_kernel(const FrameAppendArgs
     if (t < T) {
       const int page = t < a.n_patch ? patch : sp;
       const int slot = t < a.n_patch ? t : it.sp_off + (t - a.n_patch);
-      *reinterpret_cast<uint4*>(row_ptr(a.pool, page, kv, h, slot) + swizzle_chunk(slot, c) * 8) =
-          val[i];
+      store_row_chunk(a.pool, page, kv, h, slot, c, val[i]);
     }
     // a freshly opened special page gets its unused slots zeroed, so that every
     // slot of a held page is a token or zero (the grid covers page_size +
     // n_special > page_size - n_special token indices)
     if (it.new_sp && t < a.pool.page_size - a.n_special) {
       const int slot = a.n_special + t;
-      *reinterpret_cast<uint4*>(row_ptr(a.pool, sp, kv, h, slot) + swizzle_chunk(slot, c) * 8) =
-          make_uint4(0u, 0u, 0u, 0u);
+      store_row_chunk(a.pool, sp, kv, h, slot, c, make_uint4(0u, 0u, 0u, 0u));
     }
   }
 }
@@ -158,7 +150,7 @@ __global__ void __launch_bounds__(512) chunk_append_kernel(const ChunkAppendArgs
       atomicOr(a.err, kErrPageRange);
       return;
     }
-    *reinterpret_cast<uint4*>(row_ptr(a.pool, page, kv, h, slot) + swizzle_chunk(slot, c) * 8) = val;
+    store_row_chunk(a.pool, page, kv, h, slot, c, val);
   };
   // tokens t0 .. t0 + TPB - 1, loads first
   const int t0 = blockIdx.x * TPB;
@@ -234,10 +226,19 @@ __global__ void __launch_bounds__(256) reset_copy_kernel(const ResetCopyArgs a) 
         continue;
       }
       const int src_slot = a.src_sp_off[ci] + j;
-      const uint16_t* src = a.pool + layer * a.layer_elems + (long long)src_page * a.page_elems +
-                            ((long long)(kv * H + h) * Ps + src_slot) * kHeadDim +
-                            swizzle_chunk(src_slot, c) * 8;
-      val = *reinterpret_cast<const uint4*>(src);
+      if (a.fp8) {
+        // FP8 pages: the row's codes (8 per chunk) and exponent move as they are
+        const uint8_t* base = reinterpret_cast<const uint8_t*>(a.pool) + layer * a.layer_bytes +
+                              (long long)src_page * a.page_bytes;
+        const long long row = (long long)(kv * H + h) * Ps + src_slot;
+        const uint2 codes = *reinterpret_cast<const uint2*>(base + row * kHeadDim + 8 * c);
+        val = make_uint4(codes.x, codes.y, c == 0 ? (uint32_t)(uint8_t)base[a.exp_off + row] : 0u, 0u);
+      } else {
+        const uint16_t* src = a.pool + layer * a.layer_elems + (long long)src_page * a.page_elems +
+                              ((long long)(kv * H + h) * Ps + src_slot) * kHeadDim +
+                              swizzle_chunk(src_slot, c) * 8;
+        val = *reinterpret_cast<const uint4*>(src);
+      }
       dst_page_k = ci / a.f_sp;
       dst_slot = (ci % a.f_sp) * a.n_special + j;
     } else {
@@ -252,6 +253,14 @@ __global__ void __launch_bounds__(256) reset_copy_kernel(const ResetCopyArgs a) 
     const int dst_page = a.free_stack[a.top - 1 - dst_page_k];
     if (!page_ok(dst_page, a.pool_pages)) {
       atomicOr(a.err, kErrPageRange);
+      continue;
+    }
+    if (a.fp8) {
+      uint8_t* base = reinterpret_cast<uint8_t*>(a.pool) + layer * a.layer_bytes +
+                      (long long)dst_page * a.page_bytes;
+      const long long row = (long long)(kv * H + h) * Ps + dst_slot;
+      *reinterpret_cast<uint2*>(base + row * kHeadDim + 8 * c) = make_uint2(val.x, val.y);
+      if (c == 0) base[a.exp_off + row] = (uint8_t)val.z;
       continue;
     }
     uint16_t* dst = a.pool + layer * a.layer_elems + (long long)dst_page * a.page_elems +

@@ -34,14 +34,20 @@ def cfg_of(w):
 
 
 class Pair:
-    def __init__(self, w, seed=0, layers=None, pool_pages=None, max_streams=64):
+    """fp8=True pairs an FP8-page cache with the oracle: the oracle then attends
+    over the keys and values as FP8 pages return them (oracle/fp8.py), and the
+    pool check compares the stored codes and row exponents."""
+
+    def __init__(self, w, seed=0, layers=None, pool_pages=None, max_streams=64, fp8=False):
         from paged_kv_cache_build_gb300 import PagedKVCache
-        self.w, self.seed = w, seed
+        self.w, self.seed, self.fp8 = w, seed, fp8
         self.layers = layers or w.layers
         self.P = pool_pages or w.pool_pages
-        self.gpu = PagedKVCache(self.P, w.page_size, w.heads, w.head_dim, self.layers, max_streams)
+        self.gpu = PagedKVCache(self.P, w.page_size, w.heads, w.head_dim, self.layers, max_streams,
+                                fp8=fp8)
         self.ora = PagedCacheOracle(self.P, w.page_size, max_streams)
         self._kv = {}
+        self._kv_seen = {}
 
     def open(self, w=None):
         g, o = cfg_of(w or self.w)
@@ -63,6 +69,7 @@ class Pair:
         return torch.cat([self.gpu_tensor(sid, layer, f, TENSOR_Q, self.w.q_scale) for f in frames])
 
     def lookup(self, sid, frame, layer):
+        """The K and V a frame appended (bf16 bits)."""
         key = (sid, frame, layer)
         if key not in self._kv:
             w = self.w
@@ -71,6 +78,18 @@ class Pair:
                              frame_tensor(self.seed, w.index, sid, layer, frame, TENSOR_V,
                                           w.frame_tokens, w.heads, w.head_dim))
         return self._kv[key]
+
+    def lookup_seen(self, sid, frame, layer):
+        """The K and V the cache returns for that frame: as appended, or (FP8
+        pages) after quantization to E4M3 codes with row exponents."""
+        if not self.fp8:
+            return self.lookup(sid, frame, layer)
+        key = (sid, frame, layer)
+        if key not in self._kv_seen:
+            from oracle.fp8 import roundtrip_rows
+            k, v = self.lookup(sid, frame, layer)
+            self._kv_seen[key] = (roundtrip_rows(k), roundtrip_rows(v))
+        return self._kv_seen[key]
 
     def cpu_q(self, sid, layer, frames):
         w = self.w
@@ -105,8 +124,21 @@ class Pair:
 
     def check_pool(self, sid, layer=0):
         """Every valid slot of every visible page holds exactly the token the
-        oracle says it holds (bitwise)."""
+        oracle says it holds (bitwise; FP8 pages: the codes and row exponents)."""
         idx, lens = self.ora.visible_table(sid)
+        if self.fp8:
+            from oracle.fp8 import quantize_rows
+            for p, n in zip(idx, lens):
+                for kv in (0, 1):
+                    codes, exps = self.gpu.read_page_fp8(p, kv, layer)
+                    for slot in range(n):
+                        s, f, t = self.ora.slots[p][slot]
+                        want_c, want_e = quantize_rows(self.lookup(s, f, layer)[kv][t])
+                        np.testing.assert_array_equal(codes[:, slot, :], want_c,
+                                                      err_msg=f"page {p} slot {slot} kv {kv} codes")
+                        np.testing.assert_array_equal(exps[:, slot], want_e,
+                                                      err_msg=f"page {p} slot {slot} kv {kv} exponents")
+            return
         for p, n in zip(idx, lens):
             for kv in (0, 1):
                 page = self.gpu.read_page(p, kv, layer)
@@ -117,7 +149,7 @@ class Pair:
                                                   err_msg=f"page {p} slot {slot} kv {kv}")
 
     def oracle_attention(self, sid, layer, q_bits, rows=None):
-        k, v = gather_visible(self.ora.visible_tokens(sid), layer, self.lookup)
+        k, v = gather_visible(self.ora.visible_tokens(sid), layer, self.lookup_seen)
         o = attend_fp64(q_bits, k, v, self.w.sm_scale, rows=rows)
         # attention-weighted mean of |v|: bounds the effect of rounding P to bf16
         e_abs_v = attend_fp64(q_bits, k, v & np.uint16(0x7FFF), self.w.sm_scale, rows=rows)
@@ -129,7 +161,7 @@ def oracle_attention_all_rows(pair, sid, layer, q_bits, block=1374, workers=8):
     threads compute side by side (the oracle itself is unchanged: each block is
     one call of attend_fp64 with its `rows`)."""
     from concurrent.futures import ThreadPoolExecutor
-    k, v = gather_visible(pair.ora.visible_tokens(sid), layer, pair.lookup)
+    k, v = gather_visible(pair.ora.visible_tokens(sid), layer, pair.lookup_seen)
     v_abs = v & np.uint16(0x7FFF)
     n = q_bits.shape[0]
     blocks = [np.arange(r, min(n, r + block)) for r in range(0, n, block)]
