@@ -54,6 +54,11 @@ def parse():
     p.add_argument("--profile-frame-attn", type=int, default=0,
                    help="run N intra-frame attention calls on a VGGT chunk's 8 x 1374-token frames "
                         "and exit (a small case for ncu)")
+    p.add_argument("--profile-long", type=int, default=0,
+                   help="run N frames of the 24-layer keyframe stream once and exit (a small case for ncu)")
+    p.add_argument("--profile-append", type=int, default=0,
+                   help="run N batched 32-stream appends (sources rotated over 8 sets) and exit")
+    p.add_argument("--fp8", action="store_true", help="with --profile-long: E4M3 pages")
     p.add_argument("--no-extra", action="store_true", help="skip the extra workload measurements")
     return p.parse_args()
 
@@ -406,6 +411,65 @@ def extra_long24(frames=240, warm=100, frame_attn=False):
             "ms_per_frame_step": round(ms / frames, 4)}
 
 
+def _percentile(xs, q):
+    xs = sorted(xs)
+    return xs[min(len(xs) - 1, int(round(q * (len(xs) - 1))))]
+
+
+def extra_long24_full(fp8=False, frames=None, chunk=500, warm=80):
+    """The 24-layer keyframe stream as configured: 10,000 frames, 256 + 6 tokens,
+    16 x 64 heads, page 256, 8 scale frames, 64-frame window, keyframe interval 4
+    (non-keyframes append, attend and roll back). Every frame runs through all 24
+    layers from native code (pkv_stream_frames_multi: per layer append + attend,
+    then evict or roll back), in calls of `chunk` frames, with a CUDA event at
+    every frame boundary: frame-steps/s over the whole stream and the p50 / p99
+    frame time. Inputs: a ring of 8 distinct frames per layer (the cache's pages
+    and work do not depend on the values). fp8: the same on E4M3 pages."""
+    import torch
+    from paged_kv_cache_build_gb300 import PagedKVCache, frame_stream_cfg, synth_fill
+    from synth import TENSOR_K, TENSOR_Q, TENSOR_V, WORKLOADS, is_keyframe
+    w = WORKLOADS["long"]
+    F = frames or w.frames
+    L, R = w.layers, 8
+    cache = PagedKVCache(w.pool_pages, w.page_size, w.heads, w.head_dim, layers=L, fp8=fp8)
+    sid = cache.open_stream(frame_stream_cfg(w.num_scale, w.window, w.n_patch, w.n_special))
+    shape = (L, R, w.frame_tokens, w.heads, w.head_dim)
+    q, k, v = (torch.empty(shape, dtype=torch.bfloat16, device="cuda") for _ in range(3))
+    out = torch.empty_like(q)
+    for layer in range(L):
+        synth_fill(q[layer], 0, w.index, 0, layer, 0, TENSOR_Q, 0, w.q_scale)
+        synth_fill(k[layer], 0, w.index, 0, layer, 0, TENSOR_K)
+        synth_fill(v[layer], 0, w.index, 0, layer, 0, TENSOR_V)
+    keys = [is_keyframe(t, w.num_scale, w.keyframe_interval) for t in range(F)]
+    qs, ks, vs, os_ = list(q), list(k), list(v), list(out)
+    if warm:
+        # warm-up on a separate stream of the same cache, then closed
+        wsid = cache.open_stream(frame_stream_cfg(w.num_scale, w.window, w.n_patch, w.n_special))
+        cache.stream_frames_multi(wsid, qs, ks, vs, os_, 0, warm, keys[:warm], sm_scale=w.sm_scale)
+        cache.close_stream(wsid)
+    torch.cuda.synchronize()
+    per_frame, total_ms = [], 0.0
+    for f0 in range(0, F, chunk):
+        n = min(chunk, F - f0)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        cache.stream_frames_multi(sid, qs, ks, vs, os_, f0, n, keys[f0:f0 + n], sm_scale=w.sm_scale,
+                                  events=ev)
+        torch.cuda.synchronize()
+        per_frame += [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+        total_ms += ev[0].elapsed_time(ev[n])
+    cache.sync()
+    n_pages, n_kv = cache.visible_count(sid)
+    cache.close()
+    kf = [t for t in range(F) if keys[t]]
+    return {"workload": "long-24layer-kf4, all %d frames (%s pages), native frame runs of %d"
+                        % (F, "E4M3" if fp8 else "bf16", chunk),
+            "frame_steps_per_s": round(F / (total_ms * 1e-3), 2),
+            "ms_per_frame_step": round(total_ms / F, 4),
+            "p50_ms": round(_percentile(per_frame, 0.5), 4), "p99_ms": round(_percentile(per_frame, 0.99), 4),
+            "keyframe_p50_ms": round(_percentile([per_frame[t] for t in kf], 0.5), 4),
+            "final_visible": {"pages": n_pages, "tokens": n_kv}}
+
+
 def extra_append(reps=20):
     """32 streams' frames appended in one batched launch (pkv_append_frames):
     2 x 262 x 16 x 64 x 2 B read and written per stream: GB/s against HBM."""
@@ -417,12 +481,17 @@ def extra_append(reps=20):
     cache = PagedKVCache(w.pool_pages, w.page_size, w.heads, w.head_dim, max_streams=64)
     sids = [cache.open_stream(frame_stream_cfg(w.num_scale, w.window, w.n_patch, w.n_special))
             for _ in range(n)]
-    kv = torch.empty((2, n, w.frame_tokens, w.heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
-    synth_fill(kv[0], 0, w.index, 0, 0, 0, TENSOR_K)
-    synth_fill(kv[1], 0, w.index, 0, 0, 0, TENSOR_V)
-    ks, vs = [kv[0, i] for i in range(n)], [kv[1, i] for i in range(n)]
+    # eight source sets (8 x 68.7 MB > L2) used in turn, so every launch reads
+    # its K/V from HBM
+    S = 8
+    kv = torch.empty((S, 2, n, w.frame_tokens, w.heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    for i in range(S):
+        synth_fill(kv[i, 0], 0, w.index, 0, 0, i * n, TENSOR_K)
+        synth_fill(kv[i, 1], 0, w.index, 0, 0, i * n, TENSOR_V)
     times = []
     for r in range(reps + 3):
+        src = kv[r % S]
+        ks, vs = [src[0, i] for i in range(n)], [src[1, i] for i in range(n)]
         e0, e1 = _events()
         torch.cuda._sleep(HOST_COVER_CYCLES)     # the host queues the call meanwhile
         e0.record()
@@ -439,7 +508,8 @@ def extra_append(reps=20):
     moved = 2.0 * 2 * n * w.frame_tokens * w.heads * w.head_dim * 2
     peaks, kind = measured_peaks()
     gbs = moved / (ms * 1e-3) / 1e9
-    return {"workload": "32-stream batched append, 256+6 tokens x 16 x 64 bf16",
+    return {"workload": "32-stream batched append, 256+6 tokens x 16 x 64 bf16, 8 source sets "
+                        "(550 MB) used in turn",
             "bytes_per_launch": int(moved), "us_per_launch": round(ms * 1e3, 2),
             "gbs": round(gbs, 1), "hbm_peak_gbs": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 3),
             "peak_source": kind}
@@ -511,6 +581,84 @@ def extra_multistream(frames=100, reps=20):
             "frame_steps_per_s_batched": round(n / (res["batched"] * 1e-3), 1),
             "frame_steps_per_s_separate": round(n / (res["separate"] * 1e-3), 1),
             "attn_tflops_batched": round(flops / (res["batched"] * 1e-3) / 1e12, 2)}
+
+
+def extra_multistream_full(steps=None):
+    """The multi-stream pool as configured: 32 LingBot-shaped streams on one pool
+    and free list, lengths U[100, 5000] and keyframe intervals from {1, 2, 4, 8}
+    (multistream_schedule(0)), windowed mode (window_size 128 KV slots, 8 overlap
+    keyframes). Each global step: one batched append of every active stream
+    (ascending ids), one batched attention of all of them (pkv_attend_batched),
+    rollbacks of the non-keyframe streams (descending), evictions (windowed resets
+    inside) of the keyframe streams (ascending); a stream closes after its last
+    frame. Inputs: a ring of 4 frames per stream. frame-steps/s counts every
+    stream's frame; attention TFLOP/s is over the batched attention calls."""
+    import ctypes
+    import torch
+    from paged_kv_cache_build_gb300 import PagedKVCache, frame_stream_cfg, synth_fill
+    from paged_kv_cache_build_gb300._lib import check
+    from synth import TENSOR_K, TENSOR_Q, TENSOR_V, WORKLOADS, is_keyframe, multistream_schedule
+    w = WORKLOADS["multistream"]
+    n, T, H, D = w.streams, w.frame_tokens, w.heads, w.head_dim
+    sched = multistream_schedule(0)
+    n_steps = max(l for l, _ in sched) if steps is None else steps
+    cache = PagedKVCache(w.pool_pages, w.page_size, H, D, max_streams=64)
+    cfg = frame_stream_cfg(w.num_scale, w.window, w.n_patch, w.n_special, w.window_slots,
+                           w.overlap_keyframes)
+    sids = [cache.open_stream(cfg) for _ in range(n)]
+    R = 4
+    kv = torch.empty((2, R, n, T, H, D), dtype=torch.bfloat16, device="cuda")
+    q = torch.empty((R, n * T, H, D), dtype=torch.bfloat16, device="cuda")
+    for r in range(R):
+        synth_fill(kv[0, r], 0, w.index, 0, 0, r * n, TENSOR_K)
+        synth_fill(kv[1, r], 0, w.index, 0, 0, r * n, TENSOR_V)
+        synth_fill(q[r].view(n, T, H, D), 0, w.index, 0, 0, r * n, TENSOR_Q, 0, w.q_scale)
+    out = torch.empty((n * T, H, D), dtype=torch.bfloat16, device="cuda")
+    lib, h = cache.lib, cache.h
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    scale = ctypes.c_float(w.sm_scale)
+    att_events, frames, flops = [], 0, 0.0
+    torch.cuda.synchronize()
+    e0, e1 = _events()
+    e0.record()
+    for g in range(n_steps):
+        active = [s for s in sids if g < sched[s][0]]
+        if not active:
+            break
+        r = g % R
+        cache.append_frames(active, [kv[0, r, s] for s in active], [kv[1, r, s] for s in active])
+        m = len(active)
+        c_off = (ctypes.c_int * (m + 1))(*[i * T for i in range(m + 1)])
+        c_sids = (ctypes.c_int * m)(*active)
+        ea, eb = _events()
+        ea.record()
+        check(lib.pkv_attend_batched(h, ctypes.c_void_p(q[r].data_ptr()), c_off, c_sids, m, 0,
+                                     ctypes.c_void_p(out.data_ptr()), scale, stream), h)
+        eb.record()
+        att_events.append((ea, eb))
+        for s in active:
+            flops += 4.0 * T * cache.visible_count(s)[1] * D * H
+        frames += m
+        keep = {s for s in active if is_keyframe(g, w.num_scale, sched[s][1])}
+        for s in sorted(active, reverse=True):
+            if s not in keep:
+                cache.rollback_last_frame(s)
+        for s in sorted(keep):
+            cache.evict_window(s)
+        for s in active:
+            if sched[s][0] == g + 1:
+                cache.close_stream(s)
+    e1.record()
+    torch.cuda.synchronize()
+    total_ms = e0.elapsed_time(e1)
+    att_ms = sum(a.elapsed_time(b) for a, b in att_events)
+    cache.sync()
+    cache.close()
+    return {"workload": "32-stream pool, schedule 0 (lengths 100-5000, kf 1/2/4/8), windowed 128 "
+                        "slots, 8 overlap keyframes, %d global steps" % len(att_events),
+            "frames": frames, "frame_steps_per_s": round(frames / (total_ms * 1e-3), 1),
+            "attn_ms_total": round(att_ms, 2), "attn_tflops": round(flops / (att_ms * 1e-3) / 1e12, 2),
+            "ms_total": round(total_ms, 2)}
 
 
 def extra_sampled(frames=150, reps=20):
@@ -810,7 +958,11 @@ def run_ours(args):
                 return fn(*a, **kw)
             except Exception as exc:                    # noqa: BLE001
                 return {"error": "%s: %s" % (type(exc).__name__, str(exc)[:200])}
-        line["extra"] = {"chunked": measured(extra_chunked), "long24": measured(extra_long24),
+        line["extra"] = {"chunked": measured(extra_chunked),
+                         "long24_full": measured(extra_long24_full),
+                         "long24_full_fp8": measured(extra_long24_full, fp8=True),
+                         "multistream_full": measured(extra_multistream_full),
+                         "long24": measured(extra_long24),
                          "append": measured(extra_append), "multistream": measured(extra_multistream),
                          "sampled": measured(extra_sampled), "frames": measured(extra_frames),
                          "model24": measured(extra_long24, frame_attn=True),
@@ -950,9 +1102,30 @@ def run_profile_frame_attn(args):
     print(json.dumps({"profile_frame_attn": args.profile_frame_attn}))
 
 
+def run_profile_long(args):
+    """N frames of the 24-layer keyframe stream (bf16 or, with --fp8, E4M3 pages)
+    through pkv_stream_frames_multi: 24 attention launches per frame."""
+    import __graft_entry__
+    __graft_entry__.build()
+    extra_long24_full(fp8=args.fp8, frames=args.profile_long, chunk=args.profile_long, warm=0)
+    print(json.dumps({"profile_long": args.profile_long, "fp8": args.fp8}))
+
+
+def run_profile_append(args):
+    """N batched appends of 32 LingBot-shaped streams, sources rotated over 8 sets."""
+    import __graft_entry__
+    __graft_entry__.build()
+    extra_append(reps=max(args.profile_append - 3, 1))
+    print(json.dumps({"profile_append": args.profile_append}))
+
+
 def main():
     args = parse()
-    if args.profile_frame_attn:
+    if args.profile_long:
+        run_profile_long(args)
+    elif args.profile_append:
+        run_profile_append(args)
+    elif args.profile_frame_attn:
         run_profile_frame_attn(args)
     elif args.profile_chunks:
         run_profile_chunked(args)

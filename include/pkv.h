@@ -239,6 +239,32 @@ pkv_status pkv_stream_frames(pkv_t h, int stream_id, int layer, const void* q, c
                              const unsigned char* keyframe, void* out, float sm_scale,
                              void* cuda_stream);
 
+/* A run of n_frames frames of one frame-mode stream through n_layers layers,
+ * driven from native code: the model-shaped step of "LingBot-Map Paged KV Cache"
+ * sections 2-3 (each layer appends the new frame's K/V and attends its queries
+ * over that layer's visible pages; the frame is then committed with
+ * pkv_evict_window when it is a keyframe, or undone with pkv_rollback_last_frame).
+ * For frame i (its index frame0 + i) it makes exactly these calls on cuda_stream:
+ *   for l in 0 .. n_layers-1:
+ *     pkv_append_frame(h, stream_id, l, k[l] + slot, v[l] + slot, tokens)
+ *     pkv_attend(h, q[l] + slot, tokens, stream_id, l, out[l] + slot, sm_scale)
+ *   keyframe == NULL || keyframe[i] ? pkv_evict_window : pkv_rollback_last_frame
+ * where slot is frame (frame0 + i) % ring of the per-layer input rings: q[l], k[l],
+ * v[l], out[l] are device bf16 [ring][tokens][heads][64] (HOST arrays of n_layers
+ * device pointers, each 16-byte aligned). keyframe: HOST array of n_frames bytes,
+ * or NULL. events: HOST array of n_frames + 1 cudaEvent_t, or NULL; events[i] is
+ * recorded on cuda_stream before frame i's calls and events[n_frames] after the
+ * last, so the caller can read each frame's device time.
+ * Errors: INVALID (null or unaligned pointer, n_layers outside 1 .. layers,
+ * n_frames < 0, ring < 1, frame0 < 0, tokens), STATE (a chunked-mode stream, or a
+ * frame of this stream is pending); else the first failing call's status, with
+ * the frame's index in pkv_last_error (the frames before it stay applied). */
+pkv_status pkv_stream_frames_multi(pkv_t h, int stream_id, int n_layers, const void* const* q,
+                                   const void* const* k, const void* const* v, int ring, int frame0,
+                                   int n_frames, int tokens, const unsigned char* keyframe,
+                                   void* const* out, float sm_scale, void* const* events,
+                                   void* cuda_stream);
+
 /* Write the visible page table (section 2, build_visible_page_table): page ids in
  * the order scale -> window (oldest first) -> special (allocation order); chunked
  * mode: chunks oldest first, pages in order.

@@ -213,6 +213,33 @@ class PagedKVCache:
                                                float(sm_scale), _stream_ptr(stream)))
         return out
 
+    def stream_frames_multi(self, sid, qs, ks, vs, outs, frame0, n_frames, keyframe=None,
+                            sm_scale=0.0, events=None, stream=None):
+        """pkv_stream_frames_multi: frames frame0 .. frame0 + n_frames - 1 through
+        len(qs) layers (append and attend per layer, then evict or roll back).
+        qs/ks/vs/outs: one [ring][tokens][heads][64] bf16 CUDA tensor per layer;
+        frame t uses slot t % ring. events: n_frames + 1 torch.cuda.Event (timing
+        enabled), recorded at the frame boundaries, or None."""
+        L = len(qs)
+        if not (len(ks) == len(vs) == len(outs) == L):
+            raise ValueError("one q, k, v and out tensor per layer")
+        ring, tokens = qs[0].shape[0], qs[0].shape[1]
+        arr = lambda ts, name: (ctypes.c_void_p * L)(*[_bf16_ptr(t, name).value for t in ts])  # noqa: E731
+        flags = None
+        if keyframe is not None:
+            if len(keyframe) != n_frames:
+                raise ValueError("one keyframe flag per frame")
+            flags = (ctypes.c_ubyte * n_frames)(*[1 if f else 0 for f in keyframe])
+        ev = None
+        if events is not None:
+            if len(events) != n_frames + 1:
+                raise ValueError("n_frames + 1 events")
+            ev = (ctypes.c_void_p * (n_frames + 1))(*[e.cuda_event for e in events])
+        self._check(self.lib.pkv_stream_frames_multi(
+            self.h, sid, L, arr(qs, "q"), arr(ks, "k"), arr(vs, "v"), ring, frame0, n_frames, tokens,
+            ctypes.cast(flags, ctypes.c_void_p) if flags else None, arr(outs, "out"), float(sm_scale),
+            ev, _stream_ptr(stream)))
+
     def attend_noalloc(self, q, sid, layer=0, out=None, sm_scale=0.0, stream=None):
         """pkv_attend_noalloc: attention whose scratch is a fixed device array."""
         if out is None:

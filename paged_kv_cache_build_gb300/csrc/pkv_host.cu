@@ -948,6 +948,54 @@ pkv_status pkv_stream_frames(pkv_t h, int sid, int layer, const void* q, const v
   return PKV_OK;
 }
 
+pkv_status pkv_stream_frames_multi(pkv_t h, int sid, int n_layers, const void* const* q,
+                                   const void* const* k, const void* const* v, int ring, int frame0,
+                                   int n_frames, int tokens, const unsigned char* keyframe,
+                                   void* const* out, float sm_scale, void* const* events,
+                                   void* cuda_stream) {
+  Stream* st = nullptr;
+  if (pkv_status r = get_stream(h, sid, &st)) return r;
+  if (st->cfg.mode != PKV_MODE_FRAME)
+    return fail(h, PKV_ERR_STATE, "pkv_stream_frames_multi needs a frame-mode stream");
+  if (st->pending) return fail(h, PKV_ERR_STATE, "a frame of stream %d is pending", sid);
+  if (n_layers < 1 || n_layers > h->L)
+    return fail(h, PKV_ERR_INVALID, "n_layers %d outside 1..%d", n_layers, h->L);
+  if (n_frames < 0 || ring < 1 || frame0 < 0)
+    return fail(h, PKV_ERR_INVALID, "n_frames %d, ring %d, frame0 %d", n_frames, ring, frame0);
+  if (tokens != st->cfg.n_patch + st->cfg.n_special)
+    return fail(h, PKV_ERR_INVALID, "tokens %d != n_patch + n_special", tokens);
+  if (n_frames == 0) return PKV_OK;
+  if (!q || !k || !v || !out) return fail(h, PKV_ERR_INVALID, "null pointer array");
+  for (int l = 0; l < n_layers; ++l)
+    if (!q[l] || !k[l] || !v[l] || !out[l] || !aligned16(q[l]) || !aligned16(k[l]) ||
+        !aligned16(v[l]) || !aligned16(out[l]))
+      return fail(h, PKV_ERR_INVALID, "layer %d: q/k/v/out must be 16-byte aligned device pointers", l);
+  cudaStream_t s = as_stream(cuda_stream);
+  const size_t fb = (size_t)tokens * h->H * kHeadDim * sizeof(uint16_t);   // bytes per frame
+  for (int i = 0; i < n_frames; ++i) {
+    if (events && events[i]) PKV_CUDA(h, cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s));
+    const size_t o = fb * (size_t)((frame0 + i) % ring);
+    pkv_status r = PKV_OK;
+    for (int l = 0; l < n_layers && r == PKV_OK; ++l) {
+      r = pkv_append_frame(h, sid, l, static_cast<const char*>(k[l]) + o,
+                           static_cast<const char*>(v[l]) + o, tokens, cuda_stream);
+      if (r == PKV_OK)
+        r = pkv_attend(h, static_cast<const char*>(q[l]) + o, tokens, sid, l,
+                       static_cast<char*>(out[l]) + o, sm_scale, cuda_stream);
+    }
+    if (r == PKV_OK)
+      r = (keyframe == nullptr || keyframe[i]) ? pkv_evict_window(h, sid, cuda_stream)
+                                               : pkv_rollback_last_frame(h, sid, cuda_stream);
+    if (r != PKV_OK) {
+      h->last_error = "frame " + std::to_string(frame0 + i) + ": " + h->last_error;
+      return r;
+    }
+  }
+  if (events && events[n_frames])
+    PKV_CUDA(h, cudaEventRecord(static_cast<cudaEvent_t>(events[n_frames]), s));
+  return PKV_OK;
+}
+
 pkv_status pkv_attend_chunked(pkv_t h, const void* q, int n_q, int sid, int layer, void* out,
                               float sm_scale, void* cuda_stream) {
   Stream* st = nullptr;

@@ -107,3 +107,46 @@ def test_errors_and_partial_runs():
     assert _state(a, sa) == _state(b, sb)
     a.sync()
     b.sync()
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_multi_layer_run_equals_separate_calls(fp8):
+    """pkv_stream_frames_multi: 3 layers, a ring of 5 input frames, keyframe
+    interval 4 (rollbacks), frame events; equal to the separate per-layer calls."""
+    from paged_kv_cache_build_gb300 import PagedKVCache, frame_stream_cfg, synth_fill
+    w = WORKLOADS["long"]
+    L, R, frames = 3, 5, 90
+    shape = (L, R, w.frame_tokens, w.heads, w.head_dim)
+    q, k, v = (torch.empty(shape, dtype=torch.bfloat16, device="cuda") for _ in range(3))
+    for layer in range(L):
+        synth_fill(q[layer], 1, w.index, 0, layer, 0, TENSOR_Q, 0, w.q_scale)
+        synth_fill(k[layer], 1, w.index, 0, layer, 0, TENSOR_K)
+        synth_fill(v[layer], 1, w.index, 0, layer, 0, TENSOR_V)
+    caches = [PagedKVCache(w.pool_pages, w.page_size, w.heads, w.head_dim, layers=L, fp8=fp8)
+              for _ in range(2)]
+    sids = [c.open_stream(frame_stream_cfg(w.num_scale, w.window, w.n_patch, w.n_special))
+            for c in caches]
+    keys = [is_keyframe(t, w.num_scale, 4) for t in range(frames)]
+    out_a = torch.zeros_like(q)
+    out_b = torch.zeros_like(q)
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(41)]
+    caches[0].stream_frames_multi(sids[0], list(q), list(k), list(v), list(out_a), 0, 40, keys[:40],
+                                  sm_scale=w.sm_scale, events=events)
+    caches[0].stream_frames_multi(sids[0], list(q), list(k), list(v), list(out_a), 40, 50, keys[40:],
+                                  sm_scale=w.sm_scale)
+    b, sb = caches[1], sids[1]
+    for t in range(frames):
+        for layer in range(L):
+            b.append_frame(sb, k[layer, t % R], v[layer, t % R], layer)
+            b.attend(q[layer, t % R], sb, layer, out=out_b[layer, t % R], sm_scale=w.sm_scale)
+        if keys[t]:
+            b.evict_window(sb)
+        else:
+            b.rollback_last_frame(sb)
+    torch.cuda.synchronize()
+    assert all(events[i].elapsed_time(events[i + 1]) > 0 for i in range(40))
+    np.testing.assert_array_equal(out_a.view(torch.int16).cpu().numpy(), out_b.view(torch.int16).cpu().numpy())
+    assert _state(caches[0], sids[0]) == _state(b, sb)
+    for c in caches:
+        c.sync()
+        c.close()
