@@ -121,7 +121,7 @@ pkv_status pkv_create_ex(int pool_pages, int page_size, int heads, int head_dim,
  * one head, K or V) is kept as 64 OCP E4M3 codes (1 sign, 4 exponent bits with
  * bias 7, 3 mantissa bits; largest magnitude 448) of v * 2^-e and one exponent
  * byte e: the smallest integer with max|v| <= 448 * 2^e (0 for a zero row),
- * codes rounded to nearest, ties to even. So a row holds decode(code) * 2^e,
+ * clamped to [-126, 126], codes rounded to nearest, ties to even. So a row holds decode(code) * 2^e,
  * which is exact in bf16, and the quantization is the format's only rounding.
  * A page takes 2 * heads * page_size * 65 bytes instead of * 128. Append,
  * rollback, eviction, the windowed reset and every attention call work as on

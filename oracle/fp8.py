@@ -17,7 +17,8 @@ neither the FP8 format nor the scale granularity. The readings here:
     tokens that are already visible; a per-row scale needs neither.
   * Scale value: a power of two 2^e (an 8-bit exponent, as microscaling's E8M0
     scale), e the smallest integer with amax <= 448 * 2^e for the row's largest
-    magnitude amax, clamped to [-127, 127]; a row of zeros takes e = 0. A power
+    magnitude amax, clamped to [-126, 126] so that 2^e and 2^-e are normal fp32
+    numbers; a row of zeros takes e = 0. A power
     of two keeps v * 2^-e exact, and dequantization decode(code) * 2^e exact in
     bf16, so quantization is the only rounding the format adds.
   * Rounding: v * 2^-e to the nearest E4M3 value, ties to the even code
@@ -72,14 +73,14 @@ def e4m3_encode(x):
 
 def row_exponent(amax):
     """Scale exponent of a row with largest magnitude amax (python float):
-    the smallest integer e with amax <= 448 * 2^e, clamped to [-127, 127];
+    the smallest integer e with amax <= 448 * 2^e, clamped to [-126, 126];
     0 for amax = 0. With amax = f * 2^k, f in [0.5, 1) and 448 = 0.875 * 2^9,
     that is e = k - 9 when f <= 0.875, else k - 8."""
     if amax == 0.0:
         return 0
     f, k = math.frexp(amax)
     e = k - 9 + (1 if f > 0.875 else 0)
-    return max(-127, min(127, e))
+    return max(-126, min(126, e))
 
 
 def _widen(bits):

@@ -234,6 +234,9 @@ class PagedKVCache:
         if events is not None:
             if len(events) != n_frames + 1:
                 raise ValueError("n_frames + 1 events")
+            for e in events:
+                if not e.cuda_event:        # torch creates the CUDA event on its first record
+                    e.record(stream)
             ev = (ctypes.c_void_p * (n_frames + 1))(*[e.cuda_event for e in events])
         self._check(self.lib.pkv_stream_frames_multi(
             self.h, sid, L, arr(qs, "q"), arr(ks, "k"), arr(vs, "v"), ring, frame0, n_frames, tokens,

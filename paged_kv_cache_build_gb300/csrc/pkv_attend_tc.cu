@@ -393,10 +393,7 @@ __device__ __forceinline__ uint64_t tile_mask(const AttendArgs& a, const uint16_
 __device__ __forceinline__ void fp8_dequant_rows(const uint8_t* codes, const int8_t* exps,
                                                  uint8_t* dst, int rows, int lane) {
   for (int r = lane; r < rows; r += 32) {
-    const int e = exps[r];
-    // 2^e as two normal fp32 factors (e may be -127)
-    const float s1 = __uint_as_float((uint32_t)(127 + (e >> 1)) << 23);
-    const float s2 = __uint_as_float((uint32_t)(127 + e - (e >> 1)) << 23);
+    const float sc = __uint_as_float((uint32_t)(127 + exps[r]) << 23);   // 2^e, e in [-126, 126]
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const uint4 in = *reinterpret_cast<const uint4*>(codes + r * kHeadDim + 16 * q);
@@ -409,8 +406,8 @@ __device__ __forceinline__ void fp8_dequant_rows(const uint8_t* codes, const int
           const uint16_t pair = (uint16_t)(w[i] >> (16 * hw));
           uint32_t h2;
           asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(h2) : "h"(pair));
-          const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * s1 * s2;
-          const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16))) * s1 * s2;
+          const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * sc;
+          const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16))) * sc;
           out[2 * i + hw] = pack_bf16(lo, hi);
         }
       }

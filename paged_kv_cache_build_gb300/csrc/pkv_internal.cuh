@@ -49,13 +49,14 @@ struct PoolView {
 // exponent e per row: the smallest integer with amax <= 448 * 2^e (amax the
 // row's largest magnitude; 0 for a zero row). With amax = f * 2^k, f in
 // [0.5, 1), and 448 = 0.875 * 2^9, e = k - 9 + (f > 0.875). bf16 inputs give e
-// in [-127, 120], so 2^-e is a normal fp32 value and v * 2^-e is exact.
+// in [-127, 120]; the exponent is clamped to [-126, 126], so that 2^e and 2^-e
+// are normal fp32 values and v * 2^-e and code * 2^e are exact.
 __device__ __forceinline__ int fp8_row_exponent(float amax) {
   if (!(amax > 0.f)) return 0;
   int k;
   const float f = frexpf(amax, &k);
   const int e = k - 9 + (f > 0.875f ? 1 : 0);
-  return e < -127 ? -127 : (e > 126 ? 126 : e);
+  return e < -126 ? -126 : (e > 126 ? 126 : e);
 }
 
 // Two floats to two E4M3 codes, round to nearest even (a in the low byte).

@@ -71,8 +71,8 @@ def test_row_exponent_is_the_smallest_that_fits(amax):
 
 def test_row_exponent_edges():
     assert row_exponent(0.0) == 0
-    assert row_exponent(1e-60) == -127                               # clamped below
-    assert row_exponent(448.0 * 2.0 ** 127) == 127
+    assert row_exponent(1e-60) == -126                               # clamped below
+    assert row_exponent(448.0 * 2.0 ** 127) == 126
     rng = np.random.default_rng(3)
     for amax in np.ldexp(rng.uniform(0.5, 1, 500), rng.integers(-100, 100, 500)):
         e = row_exponent(float(amax))
