@@ -22,8 +22,8 @@
 //                copy (cp.async.bulk.tensor) whose 128-byte swizzle gives the
 //                same operand layout.
 //   warps 3, 1   MMA issuers (one thread each, one per M-tile): S_m = Q_m K^T
-//                (N = 64 slots) into one of two TMEM buffers, and O_m += P_m V
-//                with P_m read from one of two TMEM buffers.
+//                (N = 64 slots) into one of three TMEM buffers, and O_m += P_m V
+//                with P_m read from the same buffer, where the softmax wrote it.
 //   warps 4..11  one warpgroup per M-tile (a thread per query row): reads its S
 //                row from TMEM, masks invalid slots, exponentiates against the
 //                row's running reference max (moved to the row max on the first
@@ -34,10 +34,9 @@
 //                every tile per warp, through warp-level mma.sync tiles held in
 //                registers; an M = 128 tensor-core tile for 6 rows would cost as
 //                much as a full one.
-// With two S and two P buffers per M-tile, QK of tile j+2 is issued as soon as
-// the softmax releases tile j, and PV of tile j runs while the softmax works on
-// tile j+1; the softmax (its exponentials) and the tensor-core queue set the
-// pace. Every mbarrier wait is bounded; a wait that gives up sets the device
+// With three S buffers per M-tile (P written in place), QK of tile j+3 is
+// issued as soon as the softmax releases tile j, and PV of tile j runs while the
+// softmax works on tile j+1; the softmax and the tensor-core queue set the pace. Every mbarrier wait is bounded; a wait that gives up sets the device
 // error word, and the CTA drains its copies and MMAs and frees TMEM before
 // returning.
 #include <cuda_bf16.h>
@@ -57,15 +56,20 @@ constexpr int kMaxMaskTiles = 512; // tiles of a CTA whose slot masks are precom
 constexpr int kStages = 8;         // KV ring depth
 constexpr int kXRows = 8;          // extra query rows handled with mma.sync
 constexpr int kXWarps = kBN / 16;  // extra-row warps: one 16-slot quarter of a tile each
-// TMEM columns: S_m buffer b (fp32) at 64 (2m + b), O_m (fp32) at 128 MT + 64m,
-// P_m buffer b (bf16 pairs, 32 columns for 64 slots) at 192 MT + 32 (2m + b);
-// 512 columns for two M-tiles, 256 for one.
+// S buffers per M-tile: tile j uses buffer j % kSBufs, and P of the tile (bf16
+// pairs) is written over the first 32 columns of its own S buffer.
+constexpr int kSBufs = 3;
+// TMEM columns: S_m buffer b (fp32, 64 columns) at 64 (kSBufs m + b), O_m (fp32)
+// at 64 kSBufs MT + 64 m; 512 columns for two M-tiles, 256 for one.
 template <int MT>
 struct TmemCols {
-  static constexpr int kO = 128 * MT;
-  static constexpr int kP = 192 * MT;
+  static __host__ __device__ constexpr int s(int m, int b) { return kBN * (kSBufs * m + b); }
+  static __host__ __device__ constexpr int o(int m) { return kBN * kSBufs * MT + kHeadDim * m; }
   static constexpr int kAlloc = MT == 1 ? 256 : 512;
 };
+static_assert(TmemCols<2>::o(1) + kHeadDim <= 512 && TmemCols<1>::o(0) + kHeadDim <= 256 &&
+                  TmemCols<2>::s(1, kSBufs - 1) + kBN <= 512,
+              "TMEM plan");
 constexpr uint32_t kSpinLimit = 1u << 25;
 // A tile is exponentiated against the running reference max; if a row's sum of
 // 2^(s - m) exceeds 2^64 (or overflows), the row's reference moves to its max.
@@ -101,9 +105,9 @@ struct __align__(1024) TcSmem {
   uint16_t kept[kMaxSampledEntries]; // a sampled call's kept table positions
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
-  uint64_t s_full[MT][2];            // S_m of the buffer's latest tile is in TMEM
-  uint64_t p_full[MT][2];            // P_m of tile j is in TMEM, S_m read, O_m rescaled (j & 1)
-  uint64_t o_done[MT];               // PV of the latest tile has completed (waited only to rescale O)
+  uint64_t s_full[MT][kSBufs];       // S_m of the buffer's latest tile is in TMEM
+  uint64_t p_full[MT][kSBufs];       // P_m of the buffer's latest tile written, O_m rescaled
+  uint64_t o_done[MT];               // a PV of the last three tiles has completed (to rescale O)
   uint64_t mma_done[MT];
   uint64_t x_done;                   // the extra-row warps have published their partials
   F8Ring<FP8> f8;
@@ -451,7 +455,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.kv_full[s], FP8 ? 2 : 1);          // copy (tx) or the two dequantizers
-      mbar_init(&sm.kv_empty[s], MT + (EXTRA ? kXWarps : 0));   // MMA issuers, extra warps
+      mbar_init(&sm.kv_empty[s], MT + (EXTRA ? kXWarps : 0));   // M-tiles (softmax), extra warps
     }
     if constexpr (FP8) {
       for (int s = 0; s < kF8Stages; ++s) {
@@ -460,10 +464,10 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
       }
     }
     for (int m = 0; m < MT; ++m) {
-      mbar_init(&sm.s_full[m][0], 1);
-      mbar_init(&sm.s_full[m][1], 1);
-      mbar_init(&sm.p_full[m][0], 4);                 // one per softmax warp of the M-tile
-      mbar_init(&sm.p_full[m][1], 4);
+      for (int b = 0; b < kSBufs; ++b) {
+        mbar_init(&sm.s_full[m][b], 1);
+        mbar_init(&sm.p_full[m][b], 4);               // one per softmax warp of the M-tile
+      }
       mbar_init(&sm.o_done[m], 1);
       mbar_init(&sm.mma_done[m], 1);
     }
@@ -733,43 +737,52 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
     // ============================================================ MMA issuers
     // One issuing thread per M-tile (warp 3: M-tile 0; warp 1: M-tile 1): an
     // issuing thread stalls on each tcgen05.mma until the tensor core takes it,
-    // and two issuers keep the tensor core twice as busy. S and P each have two
-    // TMEM buffers per M-tile, tile j using buffer j & 1. Per M-tile:
-    //   QK(m, 0), QK(m, 1) up front; then for every tile j, once the softmax
-    //   has read S and written P of tile j:
-    //   PV(m, j)      O_m += P_m V, then one arrival on the stage of tile j;
-    //   QK(m, j + 2)  into the S buffer tile j has just released, so S of the
-    //                 next tile is ready long before the softmax reaches it.
+    // and two issuers keep the tensor core twice as busy. Each M-tile has three
+    // S buffers in TMEM, tile j using buffer j % 3, its P written over the
+    // buffer's first 32 columns. Per M-tile:
+    //   QK(m, 0..2) up front; then for every tile j, once the softmax has read S
+    //   and written P of tile j:
+    //   PV(m, j)      O_m += P_m V;
+    //   QK(m, j + 3)  into the buffer of tile j, so S of the next two tiles is
+    //                 in TMEM while the softmax works and the loop from one
+    //                 tile's P to the S it releases spans three tiles.
     if (lane == 0) {
       const int m = warp == kMmaWarp ? 0 : 1;
       constexpr uint32_t kIdQK = idesc_bf16(128, kBN, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, kHeadDim, true);
       const uint64_t qa = sdesc(smem_u32(&sm.q[m][0]));
-      const uint32_t t_o = tmem + TmemCols<MT>::kO + m * kHeadDim;
+      const uint32_t t_o = tmem + TmemCols<MT>::o(m);
       auto issue_qk = [&](int j) -> bool {
         if (!mbar_wait(&sm.kv_full[j % kStages], (j / kStages) & 1, abort, a.err)) return false;
         tc_fence_after();
         const uint64_t kb = sdesc(smem_u32(&sm.k[j % kStages][0]));
-        const uint32_t t_s = tmem + kBN * (2 * m + (j & 1));
+        const uint32_t t_s = tmem + TmemCols<MT>::s(m, j % kSBufs);
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk)
           tc_mma(t_s, qa + 2 * kk, kb + 2 * kk, kIdQK, kk > 0);
-        tc_commit(&sm.s_full[m][j & 1]);
+        tc_commit(&sm.s_full[m][j % kSBufs]);
         return true;
       };
-      bool ok = nT < 1 || issue_qk(0);
-      ok = ok && (nT < 2 || issue_qk(1));
+      bool ok = true;
+      for (int j = 0; ok && j < kSBufs && j < nT; ++j) ok = issue_qk(j);
       for (int j = 0; ok && j < nT; ++j) {
-        if (!mbar_wait(&sm.p_full[m][j & 1], (j >> 1) & 1, abort, a.err)) break;
+        if (!mbar_wait(&sm.p_full[m][j % kSBufs], (j / kSBufs) & 1, abort, a.err)) break;
         tc_fence_after();
         const uint64_t vb = sdesc(smem_u32(&sm.v[j % kStages][0]));
-        const uint32_t t_p = tmem + TmemCols<MT>::kP + (kBN / 2) * (2 * m + (j & 1));
+        const uint32_t t_p = tmem + TmemCols<MT>::s(m, j % kSBufs);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           tc_mma_ts(t_o, t_p + 8 * kk, vb + 128 * kk, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&sm.o_done[m]);
-        tc_commit(&sm.kv_empty[j % kStages]);
-        if (j + 2 < nT && !issue_qk(j + 2)) break;
+        // QK(j + 3) overwrites P of tile j: the tensor core runs this thread's
+        // MMAs in issue order, so PV(j) has read P before it. Its commit (S of
+        // tile j + 3) also announces that PV(j) has completed, which frees the
+        // stage of tile j and lets O be rescaled; the last three PVs, which no
+        // QK follows, are announced on o_done.
+        if (j + kSBufs < nT) {
+          if (!issue_qk(j + kSBufs)) break;
+        } else {
+          tc_commit(&sm.o_done[m]);
+        }
       }
       // every MMA issued by this thread has completed once mma_done[m] flips
       tc_commit(&sm.mma_done[m]);
@@ -783,29 +796,45 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
     const int row = row0 + m * 128 + r;
     const bool warp_active = row0 + m * 128 + wq * 32 < a.n_q;
     const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
-    const uint32_t t_o = tmem + t_lane + TmemCols<MT>::kO + m * kHeadDim;
+    const uint32_t t_o = tmem + t_lane + TmemCols<MT>::o(m);
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;          // running max (log2 units) and sum
     bool alive = true;
-    // One wait per tile, for S of the tile. The issuing thread issues QK(j) after
-    // PV(j - 2), and the commit that announces S(j) covers every MMA it issued
-    // before, so S(j) also means that PV(j - 2), the last reader of the P buffer
-    // tile j writes, has completed. PV(j - 1) is waited for only when O must be
-    // rescaled: a parity wait on o_done phase j - 1 is exact during tile j,
-    // since phase j - 2 has completed (S(j)) and phase j cannot start before
-    // this warp arrives. The arrivals of tile j go to p_full[m][j & 1]: a warp
-    // that runs ahead to tile j + 1 arrives on the other barrier, and it reaches
-    // tile j + 2 only through S(j + 2), which the issuer starts after it has
-    // seen all four arrivals of tile j, so no phase mixes two tiles.
-    for (int j = 0; j < nT; ++j) {
-      const uint32_t t_s = tmem + t_lane + kBN * (2 * m + (j & 1));
-      if (!mbar_wait(&sm.s_full[m][j & 1], (j >> 1) & 1, abort, a.err)) {
+    // One wait per tile, for S of the tile (buffer b = j % 3, phase (j / 3) & 1).
+    // The issuing thread issues QK(j) after PV(j - 3), and the commit that
+    // announces S(j) covers every MMA it issued before, so S(j) also means that
+    // PV(j - 3) has completed: the M-tile's first thread then releases the KV
+    // stage of tile j - 3 (when a later tile needs it). PV(j - 1), and with it
+    // every earlier PV, is waited for only when O must be rescaled: through S of
+    // tile j + 2 (issued right after PV(j - 1)), or, for the last three tiles,
+    // through o_done, whose phases are the PVs of those tiles; at most the
+    // phases of PV(j - 2) and PV(j - 1) are open then, so waiting for them in
+    // order is exact. The arrivals of tile j go to p_full[m][b]: a warp running
+    // ahead arrives on the other buffers' barriers, and it reaches tile j + 3
+    // only through S(j + 3), which the issuer starts after it has seen all four
+    // arrivals of tile j, so no phase mixes two tiles.
+    const int tail0 = nT > kSBufs ? nT - kSBufs : 0;   // first PV announced on o_done
+    auto wait_pv = [&](int jj) -> bool {               // PV(jj) (and all before) done
+      if (jj + kSBufs < nT)
+        return mbar_wait(&sm.s_full[m][jj % kSBufs], (uint32_t)((jj / kSBufs + 1) & 1), abort,
+                         a.err);
+      if (jj - 1 >= tail0 && !mbar_wait(&sm.o_done[m], (uint32_t)((jj - 1 - tail0) & 1), abort, a.err))
+        return false;
+      return mbar_wait(&sm.o_done[m], (uint32_t)((jj - tail0) & 1), abort, a.err);
+    };
+    int b = 0;
+    uint32_t ph = 0;
+    for (int j = 0; j < nT; ++j, b = b == kSBufs - 1 ? 0 : b + 1, ph ^= (b == 0)) {
+      const uint32_t t_s = tmem + t_lane + TmemCols<MT>::s(m, b);
+      if (!mbar_wait(&sm.s_full[m][b], ph, abort, a.err)) {
         alive = false;
         break;
       }
+      if (wq == 0 && lane == 0 && j >= kSBufs && j - kSBufs + kStages < nT)
+        mbar_arrive(&sm.kv_empty[(j - kSBufs) % kStages]);
       tc_fence_after();
       const uint64_t bits = j < kMaxMaskTiles ? sm.tmask[j] : tile_mask<kDense>(a, sm.kept, t0 + j);
-      const uint32_t t_p = tmem + t_lane + TmemCols<MT>::kP + (kBN / 2) * (2 * m + (j & 1));
+      const uint32_t t_p = t_s;                    // P over the S columns just read
       bool rescale = false;
       float alpha = 1.f;
       if (warp_active) {
@@ -878,14 +907,14 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
           }
         }
         l_run += sum0 + sum1;
-        // P into its buffer (PV of tile j - 2, which read it, has completed)
+        // P over the first half of the S buffer (all of S is in registers)
         PKV_TMEM_ST32(t_p, pk);
         tmem_wait_st();
       }
       if (__any_sync(0xffffffffu, rescale)) {
         // O_m *= alpha for this row (alpha = 1 for rows that keep their max),
         // once PV(j - 1) has completed
-        if (j > 0 && !mbar_wait(&sm.o_done[m], (j - 1) & 1, abort, a.err)) {
+        if (j > 0 && !wait_pv(j - 1)) {
           alive = false;
           break;
         }
@@ -904,7 +933,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
       // S_m read, P_m written, O_m rescaled: PV(m, j) and QK(m, j + 2) may go
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full[m][j & 1]);
+      if (lane == 0) mbar_arrive(&sm.p_full[m][b]);
     }
     // ---- epilogue: O_m row (64 columns, one TMEM read) to the output or the split's partial
     const bool have_o = alive && nT > 0 && mbar_wait(&sm.mma_done[m], 0, abort, a.err);
