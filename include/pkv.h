@@ -105,9 +105,11 @@ pkv_status pkv_create(int pool_pages, int page_size, int heads, int head_dim, pk
  * layers share one page table, so a page id names the same page in every layer,
  * and the metadata is updated once per frame) and room for
  * `max_streams` concurrent streams sharing the pool and its free list.
- * Allocates layers*pool_pages*2*heads*page_size*head_dim bf16 (zeroed). The free
- * list is a stack that initially hands out pages 0, 1, 2, ... *out receives the
- * handle, which the caller releases with pkv_destroy.
+ * Allocates layers*pool_pages*2*heads*page_size*head_dim bf16 (zeroed), plus, for
+ * pkv_attend_blocksparse, a cache of each page's mean key per layer (fp32,
+ * layers*pool_pages*heads*head_dim values: 1/page_size of the pool's bytes) and a
+ * few KB of scratch. The free list is a stack that initially hands out pages
+ * 0, 1, 2, ... *out receives the handle, which the caller releases with pkv_destroy.
  * Errors: INVALID (null out; head_dim != 64; page_size not a multiple of 16 in
  * 16..256 that divides or is divisible by 64; pool_pages, heads (<= 32), layers or
  * max_streams (<= 1024) out of range); OOM or CUDA if the device allocations fail
@@ -346,7 +348,13 @@ pkv_status pkv_attend_frames(pkv_t h, const void* q, const void* k, const void* 
  * The attention is pkv_attend's over the kept pages' valid slots, in table order.
  * keep >= 0 (at least the number of non-anchor pages keeps them all). The
  * estimate, the selection and the attention all run on the device (no host
- * round trip); the first call allocates a small device buffer.
+ * round trip, no allocation). A page's km depends only on its rows, so the handle
+ * keeps it per layer and page, computed at the page's valid length: the append and
+ * the windowed reset drop the cached value of every page they write, and a call
+ * recomputes only pages whose cached length differs from their valid length (at
+ * steady state the current frame's pages); cached and recomputed values are the
+ * same bits. The handle's estimate scratch is shared by its calls: calls on one
+ * handle must not overlap in time (on different CUDA streams).
  * Errors: as pkv_attend; STATE for a chunked-mode stream; INVALID for keep < 0,
  * more than 1024 visible pages, or an FP8 cache. */
 pkv_status pkv_attend_blocksparse(pkv_t h, const void* q, int n_q, int stream_id, int layer,

@@ -73,7 +73,9 @@ struct pkv_ctx {
   int device = 0;                // the device current at pkv_create_ex
   float* noalloc_scratch = nullptr;   // device address of the static scratch on `device`
   void* d_select = nullptr;      // page skipping: query means, page estimates, kept list
-  int select_kept = 0;           // entries in that kept list (the last call's)
+  float* d_km = nullptr;         // bf16 pages: mean key per (layer, page, head, d)
+  int* d_km_len = nullptr;       // its tags per (layer, page): valid length, or -1
+  int select_kept = -1;          // entries in that kept list (the last call's); -1: none yet
   int num_sms = 0;
   std::string last_error;
 };
@@ -127,6 +129,7 @@ inline PoolView pool_view(pkv_t h, int layer) {
   pv.fp8 = h->fp8;
   pv.page_bytes = h->page_bytes;
   pv.exp_off = h->exp_off;
+  pv.km_len = h->d_km_len ? h->d_km_len + (long long)layer * h->P : nullptr;
   return pv;
 }
 
@@ -297,6 +300,20 @@ static pkv_status create_cache(int pool_pages, int page_size, int heads, int hea
   if (e == cudaSuccess) e = cudaMalloc(&h->d_err, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
   if (e == cudaSuccess) {
+    // page skipping's scratch (query means, estimates, kept list)
+    const size_t bytes = sizeof(float) * (kMaxHeads * kHeadDim + kMaxSampledEntries) +
+                         sizeof(uint16_t) * kMaxSampledEntries + sizeof(unsigned);
+    e = cudaMalloc(&h->d_select, bytes);
+    if (e == cudaSuccess) e = cudaMemset(h->d_select, 0, bytes);
+  }
+  if (e == cudaSuccess && !fp8) {
+    // the mean-key cache of page skipping (1 / page_size of the pool's bytes),
+    // every tag -1 (nothing cached)
+    e = cudaMalloc(&h->d_km, sizeof(float) * (size_t)layers * pool_pages * heads * head_dim);
+    if (e == cudaSuccess) e = cudaMalloc(&h->d_km_len, sizeof(int) * (size_t)layers * pool_pages);
+    if (e == cudaSuccess) e = cudaMemset(h->d_km_len, 0xFF, sizeof(int) * (size_t)layers * pool_pages);
+  }
+  if (e == cudaSuccess) {
     // free stack bottom..top = P-1 .. 0, so pops hand out 0, 1, 2, ...
     std::vector<int32_t> init(pool_pages);
     for (int i = 0; i < pool_pages; ++i) init[i] = pool_pages - 1 - i;
@@ -335,6 +352,8 @@ pkv_status pkv_destroy(pkv_t h) {
   if (h->d_err) cudaFree(h->d_err);
   if (h->d_scratch) cudaFree(h->d_scratch);
   if (h->d_select) cudaFree(h->d_select);
+  if (h->d_km) cudaFree(h->d_km);
+  if (h->d_km_len) cudaFree(h->d_km_len);
   delete h;
   return PKV_OK;
 }
@@ -746,6 +765,7 @@ static pkv_status window_reset(pkv_t h, Stream* st, cudaStream_t s) {
   ca.top = h->free_top;
   ca.n_carry = n_carry;
   ca.n_new = n_new;
+  ca.km_len = h->d_km_len;
   ca.err = h->d_err;
   for (int i = 0; i < n_carry; ++i) {
     const int j = n_held - n_carry + i;   // held position
@@ -1065,16 +1085,10 @@ pkv_status pkv_attend_blocksparse(pkv_t h, const void* q, int n_q, int sid, int 
   if (np > kMaxSampledEntries)
     return fail(h, PKV_ERR_INVALID, "%d visible pages; this call takes at most %d", np,
                 kMaxSampledEntries);
-  if (!h->d_select) {
-    const size_t bytes = sizeof(float) * (kMaxHeads * kHeadDim + kMaxSampledEntries) +
-                         sizeof(uint16_t) * kMaxSampledEntries +
-                         sizeof(float) * (size_t)kMaxSampledEntries * kMaxHeads * kHeadDim;
-    PKV_CUDA(h, cudaMalloc(&h->d_select, bytes));
-  }
   float* qm = static_cast<float*>(h->d_select);
   float* scores = qm + kMaxHeads * kHeadDim;
   uint16_t* kept = reinterpret_cast<uint16_t*>(scores + kMaxSampledEntries);
-  float* prod = reinterpret_cast<float*>(kept + kMaxSampledEntries);   // 16-byte aligned
+  unsigned* done = reinterpret_cast<unsigned*>(kept + kMaxSampledEntries);   // 4-byte aligned
   const int n_anchor = a.tbl.n_scale;
   const int n_kept = n_anchor + std::min(keep, np - n_anchor);
   PageScoreArgs g;
@@ -1089,8 +1103,10 @@ pkv_status pkv_attend_blocksparse(pkv_t h, const void* q, int n_q, int sid, int 
   g.keep = keep;
   g.qm = qm;
   g.scores = scores;
-  g.prod = prod;
+  g.km = h->d_km + (long long)layer * h->P * h->H * kHeadDim;
+  g.km_len = h->d_km_len + (long long)layer * h->P;
   g.kept = kept;
+  g.done = done;
   g.err = h->d_err;
   cudaStream_t s = as_stream(cuda_stream);
   PKV_CUDA(h, launch_page_select(g, s));
@@ -1115,7 +1131,7 @@ pkv_status pkv_attend_blocksparse(pkv_t h, const void* q, int n_q, int sid, int 
 
 pkv_status pkv_blocksparse_kept(pkv_t h, int* kept_out, int capacity, int* n_out) {
   if (!h || !kept_out || !n_out) return fail(h, PKV_ERR_INVALID, "null argument");
-  if (!h->d_select) return fail(h, PKV_ERR_STATE, "no pkv_attend_blocksparse call yet");
+  if (h->select_kept < 0) return fail(h, PKV_ERR_STATE, "no pkv_attend_blocksparse call yet");
   if (capacity < h->select_kept)
     return fail(h, PKV_ERR_INVALID, "capacity %d < %d entries", capacity, h->select_kept);
   std::vector<uint16_t> tmp(h->select_kept);

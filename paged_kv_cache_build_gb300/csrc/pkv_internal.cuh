@@ -41,6 +41,8 @@ struct PoolView {
   int fp8;                // 1: E4M3 pages
   long long page_bytes;   // bytes per page (either format)
   long long exp_off;      // FP8 pages: byte offset of the exponents in a page
+  int* km_len;            // bf16 pages: this layer's mean-key cache tags (per page), or null;
+                          // a kernel that writes a page's rows sets its tag to -1
 };
 
 // ------------------------------------------------------------- FP8 rows
@@ -185,6 +187,7 @@ struct ResetCopyArgs {              // copy carried frames' special tokens, all 
   int src_sp_idx[kMaxCarry];        // special list index of carried frame i
   int src_sp_off[kMaxCarry];        // its first slot there
   int n_new;                        // special pages the reset pops
+  int* km_len;                      // [layers][pool_pages] mean-key cache tags, or null
   int* err;
 };
 
@@ -372,8 +375,10 @@ struct PageScoreArgs {
   int keep;
   float* qm;                        // [heads][64] scratch
   float* scores;                    // [n_entries] scratch
-  float* prod;                      // [n_entries][heads][64] scratch: qm * km per page
+  float* km;                        // this layer's mean-key cache: [pool_pages][heads][64]
+  int* km_len;                      // its tags: the valid length km was computed at, or -1
   uint16_t* kept;                   // [n_anchor + keep] out
+  unsigned* done;                   // score blocks finished (0 between calls)
   int* err;
 };
 cudaError_t launch_page_select(const PageScoreArgs& a, cudaStream_t s);

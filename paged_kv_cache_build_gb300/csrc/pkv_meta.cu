@@ -86,9 +86,16 @@ __global__ void __launch_bounds__(512) frame_append_kernel(const FrameAppendArgs
       if (!ok) {
         atomicOr(a.err, kErrPageRange);
         patch = -1;
-      } else if (a.is_meta && blockIdx.x == 0) {
-        *it.patch_slot = patch;
-        if (it.new_sp) it.special_list[it.sp_idx] = sp;
+      } else {
+        if (a.is_meta && blockIdx.x == 0) {
+          *it.patch_slot = patch;
+          if (it.new_sp) it.special_list[it.sp_idx] = sp;
+        }
+        // the rows of both pages change: their cached mean keys are stale
+        if (blockIdx.x == 0 && a.pool.km_len) {
+          a.pool.km_len[patch] = -1;
+          a.pool.km_len[sp] = -1;
+        }
       }
       s_patch = patch;
       s_sp = sp;
@@ -199,6 +206,12 @@ __global__ void __launch_bounds__(256) push_kernel(const PushArgs a) {
 // those pages' unused slots.
 __global__ void __launch_bounds__(256) reset_copy_kernel(const ResetCopyArgs a) {
   const int H = a.heads, Ps = a.page_size;
+  // the popped pages' rows change: their cached mean keys are stale
+  if (blockIdx.x == 0 && a.km_len)
+    for (int i = threadIdx.x; i < a.layers * a.n_new; i += blockDim.x) {
+      const int p = a.free_stack[a.top - 1 - i % a.n_new];
+      if (page_ok(p, a.pool_pages)) a.km_len[(long long)(i / a.n_new) * a.pool_pages + p] = -1;
+    }
   const long long per_slot = 2LL * H * kChunksPerRow;
   const long long copy_total = (long long)a.layers * a.n_carry * a.n_special * per_slot;
   const long long zero_total = (long long)a.layers * a.n_new * Ps * per_slot;

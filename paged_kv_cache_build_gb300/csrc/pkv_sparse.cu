@@ -15,6 +15,12 @@
 //   km[h][d] = (sum over valid slots s in order of K[s][h][d]) / len
 //   score    = sum over h, then d, in order of (qm[h][d] * km[h][d])
 // (__fadd_rn / __fmul_rn / __fdiv_rn: no contraction into fused multiply-adds).
+// A page's km depends only on its rows, so each layer keeps a cache of km per
+// page, tagged with the valid length it was computed at; the append and the
+// windowed reset clear the tag of every page they write, and a call recomputes
+// only the pages whose tag differs from their length (at steady state the
+// frame's newest pages): two launches in all (the means; the scores and the
+// selection).
 #include <cuda_bf16.h>
 
 #include "pkv_internal.cuh"
@@ -23,107 +29,69 @@ namespace pkv {
 
 namespace {
 
-__device__ __forceinline__ float bf16_at(const uint16_t* p) {
-  return __uint_as_float((uint32_t)__ldg(p) << 16);
-}
-
-// qm[h][d]: block h; the rows go through shared memory in chunks (coalesced,
-// many loads in flight), then thread d adds its column in row order
-constexpr int kPoolRows = 128;
-__global__ void __launch_bounds__(256) pool_q_kernel(const PageScoreArgs a) {
+// The means, block (x, h), 256 threads: x = n_entries computes qm[h]; x < n_entries
+// recomputes km[h] of visible page x into the layer's mean-key cache if the
+// page's tag differs from its valid length (else it has nothing to do). The rows
+// go through shared memory (coalesced, many loads in flight), then thread d adds
+// its column in row order. The tags are set by the next launch, which reads
+// them after every block here has finished.
+constexpr int kPoolRows = 320;
+__global__ void __launch_bounds__(256) page_means_kernel(const PageScoreArgs a) {
   pdl_wait();
   pdl_trigger();
-  __shared__ uint4 rows[kPoolRows * kChunksPerRow];       // 128 rows x 64 bf16
-  const int h = blockIdx.x;
+  __shared__ uint4 rows[kPoolRows * kChunksPerRow];       // 320 rows x 64 bf16 (40 KB)
+  const int e = blockIdx.x, h = blockIdx.y;
+  const bool is_q = e == a.n_entries;
+  int page = 0, len = a.n_q;
+  if (!is_q) {
+    table_entry(a.tbl, e, page, len);
+    // a bad entry is reported by the score kernel
+    if (page < 0 || page >= a.pool.pool_pages || len < 1 || len > a.pool.page_size) return;
+    if (a.km_len[page] == len) return;
+  }
+  const uint16_t* plane = is_q ? a.q + (long long)h * kHeadDim
+                               : a.pool.base + (long long)page * a.pool.page_elems +
+                                     (long long)h * a.pool.page_size * kHeadDim;
+  const long long row_stride = is_q ? (long long)a.heads * kHeadDim : kHeadDim;
   float acc = 0.f;
-  for (int r0 = 0; r0 < a.n_q; r0 += kPoolRows) {
-    const int nr = min(kPoolRows, a.n_q - r0);
+  for (int r0 = 0; r0 < len; r0 += kPoolRows) {
+    const int nr = min(kPoolRows, len - r0);
     for (int i = threadIdx.x; i < nr * kChunksPerRow; i += blockDim.x)
-      rows[i] = __ldg(reinterpret_cast<const uint4*>(
-                          a.q + ((long long)(r0 + i / kChunksPerRow) * a.heads + h) * kHeadDim) +
+      rows[i] = __ldg(reinterpret_cast<const uint4*>(plane + (r0 + i / kChunksPerRow) * row_stride) +
                       i % kChunksPerRow);
     __syncthreads();
     if (threadIdx.x < kHeadDim) {
-      const uint16_t* base = reinterpret_cast<const uint16_t*>(rows) + threadIdx.x;
+      const int d = threadIdx.x;
+      const uint16_t* base = reinterpret_cast<const uint16_t*>(rows);
 #pragma unroll 8
-      for (int r = 0; r < nr; ++r)
-        acc = __fadd_rn(acc, __uint_as_float((uint32_t)base[r * kHeadDim] << 16));
+      for (int r = 0; r < nr; ++r) {
+        // page rows are 128-byte swizzled: value d of slot s sits in chunk
+        // swizzle_chunk(s, d / 8)
+        const int col = is_q ? d : swizzle_chunk(r0 + r, d >> 3) * 8 + (d & 7);
+        acc = __fadd_rn(acc, __uint_as_float((uint32_t)base[r * kHeadDim + col] << 16));
+      }
     }
     __syncthreads();
   }
-  if (threadIdx.x < kHeadDim)
-    a.qm[h * kHeadDim + threadIdx.x] = __fdiv_rn(acc, (float)a.n_q);
-}
-
-// prod[e][h][d] = qm[h][d] * km[h][d] for page e (blockIdx.x), head h
-// (blockIdx.y): the page's plane of head h (len rows of 128 bytes, swizzled) is
-// copied to shared memory, then thread d adds its column in slot order
-__global__ void __launch_bounds__(kHeadDim) pool_k_kernel(const PageScoreArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ uint4 plane[kMaxPageSize * kChunksPerRow];   // up to 256 rows x 64 bf16
-  const int e = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
-  int page = 0, len = 0;
-  table_entry(a.tbl, e, page, len);
-  const bool ok = page >= 0 && page < a.pool.pool_pages && len >= 1 && len <= a.pool.page_size;
-  float km = __int_as_float(0x7fc00000);                  // NaN: ranks lowest
-  if (ok) {
-    const uint4* src = reinterpret_cast<const uint4*>(
-        a.pool.base + (long long)page * a.pool.page_elems + (long long)h * a.pool.page_size * kHeadDim);
-    for (int i = d; i < len * kChunksPerRow; i += blockDim.x) plane[i] = __ldg(src + i);
-  } else if (d == 0) {
-    atomicOr(a.err, kErrPageRange);
-  }
-  __syncthreads();
-  if (ok) {
-    const uint16_t* p = reinterpret_cast<const uint16_t*>(plane) + (d & 7);
-    float acc = 0.f;
-#pragma unroll 8
-    for (int s = 0; s < len; ++s)
-      acc = __fadd_rn(acc, __uint_as_float((uint32_t)p[s * kHeadDim + swizzle_chunk(s, d >> 3) * 8]
-                                           << 16));
-    km = __fdiv_rn(acc, (float)len);
-  }
-  a.prod[((long long)e * a.heads + h) * kHeadDim + d] = __fmul_rn(a.qm[h * kHeadDim + d], km);
-}
-
-// score of page e (block e): the products in (h, d) order, one running sum
-__global__ void __launch_bounds__(256) page_score_kernel(const PageScoreArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ __align__(16) float prod[kMaxHeads * kHeadDim];
-  const int e = blockIdx.x, n = a.heads * kHeadDim;   // a multiple of 64
-  for (int i = threadIdx.x; i < n; i += blockDim.x) prod[i] = a.prod[(long long)e * n + i];
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    // the loads run ahead four at a time; the adds stay in order
-    const float4* p4 = reinterpret_cast<const float4*>(prod);
-    float acc = 0.f;
-#pragma unroll 4
-    for (int i = 0; i < n / 4; ++i) {
-      const float4 v = p4[i];
-      acc = __fadd_rn(acc, v.x);
-      acc = __fadd_rn(acc, v.y);
-      acc = __fadd_rn(acc, v.z);
-      acc = __fadd_rn(acc, v.w);
-    }
-    a.scores[e] = acc;
+  if (threadIdx.x < kHeadDim) {
+    const float v = __fdiv_rn(acc, (float)len);
+    if (is_q) a.qm[h * kHeadDim + threadIdx.x] = v;
+    else a.km[((long long)page * a.heads + h) * kHeadDim + threadIdx.x] = v;
   }
 }
 
-// kept table positions in table order: the anchors, then the `keep` best others
-__global__ void __launch_bounds__(kMaxSampledEntries) select_kernel(const PageScoreArgs a) {
-  pdl_wait();
-  pdl_trigger();
+// Kept table positions in table order: the anchors, then the `keep` best others
+// (one block; every thread takes entries e, e + blockDim.x, ...).
+__device__ void select_kept(const PageScoreArgs& a) {
   __shared__ float key[kMaxSampledEntries];
   __shared__ int flag[kMaxSampledEntries];
-  const int e = threadIdx.x, n = a.n_entries;
-  if (e < n) {
-    const float s = a.scores[e];
+  const int n = a.n_entries;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const float s = __ldcg(a.scores + e);
     key[e] = isnan(s) ? -INFINITY : s;
   }
   __syncthreads();
-  if (e < n) {
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
     int kept = 1;
     if (e >= a.n_anchor) {
       int rank = 0;
@@ -134,22 +102,74 @@ __global__ void __launch_bounds__(kMaxSampledEntries) select_kernel(const PageSc
     flag[e] = kept;
   }
   __syncthreads();
-  if (e < n && flag[e]) {
-    int pos = 0;
-    for (int o = 0; o < e; ++o) pos += flag[o];
-    a.kept[pos] = (uint16_t)e;
+  for (int e = threadIdx.x; e < n; e += blockDim.x)
+    if (flag[e]) {
+      int pos = 0;
+      for (int o = 0; o < e; ++o) pos += flag[o];
+      a.kept[pos] = (uint16_t)e;
+    }
+}
+
+// Score of page e (block e): the products qm * km of its cached mean keys (all
+// threads), added in (h, d) order as one running sum (one thread); the page's
+// tag becomes its valid length (every stale km was recomputed by the launch
+// before). A recomputed km is the same fp32 value as a cached one, bit for bit
+// (same operations, same order), and every kernel that writes a page's rows sets
+// its tag to -1, so a cached value is used only while the page's rows are the
+// ones it was computed from. The block that finishes last (a counter, after a
+// fence; no block waits for another) selects the kept pages and resets the
+// counter for the next call.
+__global__ void __launch_bounds__(256) page_score_kernel(const PageScoreArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ __align__(16) float prod[kMaxHeads * kHeadDim];
+  __shared__ int s_last;
+  const int e = blockIdx.x, n = a.heads * kHeadDim;   // n: a multiple of 64
+  int page = 0, len = 0;
+  table_entry(a.tbl, e, page, len);
+  const bool ok = page >= 0 && page < a.pool.pool_pages && len >= 1 && len <= a.pool.page_size;
+  if (ok) {
+    // the products, all at once; then one thread adds them in (h, d) order
+    const float* cache = a.km + (long long)page * n;
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+      prod[i] = __fmul_rn(__ldcg(a.qm + i), __ldcg(cache + i));
   }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float acc = __int_as_float(0x7fc00000);               // NaN: ranks lowest
+    if (ok) {
+      a.km_len[page] = len;
+      const float4* p4 = reinterpret_cast<const float4*>(prod);
+      acc = 0.f;
+#pragma unroll 8
+      for (int i = 0; i < n / 4; ++i) {
+        const float4 v = p4[i];
+        acc = __fadd_rn(acc, v.x);
+        acc = __fadd_rn(acc, v.y);
+        acc = __fadd_rn(acc, v.z);
+        acc = __fadd_rn(acc, v.w);
+      }
+    } else {
+      atomicOr(a.err, kErrPageRange);
+    }
+    a.scores[e] = acc;
+    __threadfence();
+    s_last = atomicAdd(a.done, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  select_kept(a);
+  if (threadIdx.x == 0) *a.done = 0u;
 }
 
 }  // namespace
 
 cudaError_t launch_page_select(const PageScoreArgs& a, cudaStream_t s) {
-  cudaError_t e = launch_pdl(pool_q_kernel, dim3(a.heads), dim3(256), 0, s, a);
-  if (e == cudaSuccess)
-    e = launch_pdl(pool_k_kernel, dim3(a.n_entries, a.heads), dim3(kHeadDim), 0, s, a);
+  cudaError_t e =
+      launch_pdl(page_means_kernel, dim3(a.n_entries + 1, a.heads), dim3(256), 0, s, a);
   if (e == cudaSuccess) e = launch_pdl(page_score_kernel, dim3(a.n_entries), dim3(256), 0, s, a);
-  if (e == cudaSuccess) e = launch_pdl(select_kernel, dim3(1), dim3(kMaxSampledEntries), 0, s, a);
-  count_launches(4);
+  count_launches(2);
   return e;
 }
 

@@ -5,13 +5,15 @@ positions must equal the oracle's bit for bit (oracle/blocksparse.py computes th
 same fp32 estimate in the same order), and the output must match the fp64 oracle
 over the kept pages; keep >= the visible pages is pkv_attend exactly."""
 
+import random
+
 import numpy as np
 import pytest
 import torch
 
 from oracle import attend_fp64, gather_visible
 from oracle.blocksparse import kept_positions, page_scores, visible_tokens_blocksparse
-from synth import WORKLOADS
+from synth import WORKLOADS, is_keyframe
 from tests.pairing import Pair, assert_close
 
 pytestmark = pytest.mark.gpu
@@ -69,6 +71,45 @@ def test_lingbot_against_oracle():
     for layer in (0, 1):
         for keep in (4, 16, 40):
             _check(pr, sid, layer, 119, keep, rows=rows)
+    pr.gpu.sync()
+
+
+@pytest.mark.parametrize("seed", [11, 12, 13])
+def test_mean_key_cache_follows_every_page_change(seed):
+    """Estimates on both layers at every frame of a stream with rollbacks,
+    evictions and windowed resets (which copy rows into freshly popped pages): a
+    call reuses the mean keys an earlier call cached for the pages that did not
+    change, and its kept list must still equal the oracle's, which recomputes
+    every page. A rolled-back frame's patch page goes back to the free stack and
+    is popped again by the next frame at the same length, so a page whose rows
+    changed without its cached value being dropped would show up here."""
+    rng = random.Random(seed)
+    S = rng.randint(1, 2)
+    w = WORKLOADS["tiny"].with_(page_size=32, n_patch=32, n_special=rng.choice([2, 4, 6]), num_scale=S,
+                                window=rng.randint(2, 4), heads=rng.choice([2, 4]),
+                                window_slots=rng.randint(S + 2, 7), overlap_keyframes=rng.randint(0, S))
+    pr = Pair(w, seed, layers=2, pool_pages=96)
+    sid = pr.open()
+    kf = rng.randint(1, 3)
+    for t in range(36):
+        pr.append(sid, t)
+        n_pages = pr.gpu.visible_count(sid)[0]
+        for layer in (0, 1):
+            keep = rng.randint(0, n_pages)
+            if t % 6 == 5:
+                _check(pr, sid, layer, t, keep)
+            else:
+                # kept lists only (the attention of the kept pages is checked above)
+                q = pr.gpu_q_chunk(sid, layer, [t])
+                pr.gpu.attend_blocksparse(q, sid, layer, keep=keep, sm_scale=w.sm_scale)
+                n_anchor = len(pr.ora._stream(sid, "frame").scale)
+                ref = kept_positions(page_scores(pr.ora, sid, layer, pr.cpu_q(sid, layer, [t]), pr.lookup),
+                                     n_anchor, keep)
+                assert pr.gpu.blocksparse_kept() == ref, f"seed {seed} frame {t} layer {layer}"
+        if is_keyframe(t, S, kf) and rng.random() > 0.2:
+            pr.evict(sid)
+        else:
+            pr.rollback(sid)
     pr.gpu.sync()
 
 
