@@ -56,16 +56,17 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const __grid_constant__
   const AttendArgs& a = pair_call(params, pair);
   const long long n_pairs = (long long)a.n_q * a.heads;
   const int S = a.num_splits;
-  // Eight splits at a time: their loads are issued together, then folded into
-  // the running max, sum and O. Every split writes its partials (an empty one
-  // as max -inf, sum 0, O 0).
+  // Up to kFold splits at a time (a frame's 9 splits in one round): their loads
+  // are issued together, then folded into the running max, sum and O. Every
+  // split writes its partials (an empty one as max -inf, sum 0, O 0).
+  constexpr int kFold = 12;
   float m_run = -INFINITY, l_sum = 0.f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < S; s0 += 8) {
-    float2 ml[8];
-    float4 ov[8];
+  for (int s0 = 0; s0 < S; s0 += kFold) {
+    float2 ml[kFold];
+    float4 ov[kFold];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kFold; ++i) {
       ml[i] = make_float2(-INFINITY, 0.f);
       ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (s0 + i < S) {
@@ -75,7 +76,7 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const __grid_constant__
       }
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kFold; ++i) {
       if (ml[i].y > 0.f) {
         const float m_new = fmaxf(m_run, ml[i].x);
         const float c = fast_exp2(m_run - m_new);     // 0 while m_run is -inf
