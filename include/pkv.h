@@ -130,10 +130,12 @@ pkv_status pkv_create_ex(int pool_pages, int page_size, int heads, int head_dim,
  * bf16 pages; the attention dequantizes each K/V tile in shared memory and
  * computes exactly what bf16 pages holding the dequantized values would give.
  * K and V must be finite with magnitude below 2^126.
- * Page layout (for callers that read the pool): per page the codes
- * [kv][head][slot][64] bytes, unswizzled, then the exponents [kv][head][slot]
- * as int8. pkv_attend_blocksparse and pkv_read_page refuse FP8 caches
- * (pkv_read_page_fp8 reads them).
+ * Page layout (for callers that read the pool): per page, [kv][head] planes of
+ * page_size rows, each plane in blocks of B = min(page_size, 64) rows: the B rows'
+ * 64 code bytes (unswizzled), then their B exponent bytes (int8), so a block is
+ * B * 65 bytes and one copy moves a block's codes with their exponents.
+ * pkv_attend_blocksparse and pkv_read_page refuse FP8 caches (pkv_read_page_fp8
+ * reads them).
  * Errors: as pkv_create_ex. */
 pkv_status pkv_create_fp8(int pool_pages, int page_size, int heads, int head_dim, int layers,
                           int max_streams, pkv_t* out);

@@ -76,14 +76,14 @@ constexpr uint32_t kSpinLimit = 1u << 25;
 constexpr float kSumLimit = 18446744073709551616.0f;   // 2^64
 
 // FP8 pages: the producer bulk-copies a tile's E4M3 codes and row exponents into
-// a staging ring; two warps dequantize them into the bf16 operand ring.
+// a staging ring, one copy per row block of K and of V (the page's layout: B rows
+// of 64 code bytes, then their B exponents); two warps dequantize them into the
+// bf16 operand ring.
 constexpr int kF8Stages = 4;
 template <bool FP8>
 struct __align__(128) F8Ring {
-  alignas(128) uint8_t k[kF8Stages][kBN * kHeadDim];   // codes, 64-byte rows (unswizzled)
-  alignas(128) uint8_t v[kF8Stages][kBN * kHeadDim];
-  alignas(128) int8_t ke[kF8Stages][kBN];               // row exponents
-  alignas(128) int8_t ve[kF8Stages][kBN];
+  alignas(128) uint8_t k[kF8Stages][kBN * (kHeadDim + 1)];   // K row blocks, as in the page
+  alignas(128) uint8_t v[kF8Stages][kBN * (kHeadDim + 1)];
   int nblk[kF8Stages];                     // page blocks copied into the stage
   uint64_t full[kF8Stages];                // the stage's copies have landed
   uint64_t free_[kF8Stages];               // both converting warps are done with it
@@ -389,19 +389,26 @@ __device__ __forceinline__ uint64_t tile_mask(const AttendArgs& a, const uint16_
   return bits;
 }
 
-// Dequantizes `rows` 64-value rows of FP8 codes (with their exponents) from a
-// staging stage into a bf16 operand tile at its 128-byte-swizzled place, two rows
-// per lane of one warp (row base + lane, base + 32 + lane). decode(code) is exact
-// in f16, f16 -> fp32 is exact, and the power-of-two scale and the final bf16
-// rounding are exact for these values (at most 4 significant bits).
-__device__ __forceinline__ void fp8_dequant_rows(const uint8_t* codes, const int8_t* exps,
-                                                 uint8_t* dst, int rows, int lane) {
+// Dequantizes `rows` 64-value rows of FP8 codes from a staging stage (row blocks
+// of B rows: the B rows' 64 code bytes, then their B exponents) into a bf16
+// operand tile at its 128-byte-swizzled place, two rows per lane of one warp (row
+// lane, lane + 32). A row's 64 codes are loaded before any is converted.
+// decode(code) is exact in f16, f16 -> fp32 is exact, and the power-of-two scale
+// and the final bf16 rounding are exact for these values (at most 4 significant
+// bits).
+__device__ __forceinline__ void fp8_dequant_rows(const uint8_t* stage, int B, uint8_t* dst, int rows,
+                                                 int lane) {
   for (int r = lane; r < rows; r += 32) {
-    const float sc = __uint_as_float((uint32_t)(127 + exps[r]) << 23);   // 2^e, e in [-126, 126]
+    const uint8_t* blk = stage + (r / B) * B * (kHeadDim + 1);
+    const int rb = r % B;
+    const float sc =
+        __uint_as_float((uint32_t)(127 + (int8_t)blk[B * kHeadDim + rb]) << 23);   // 2^e, |e| <= 126
+    uint4 in[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) in[q] = *reinterpret_cast<const uint4*>(blk + rb * kHeadDim + 16 * q);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint4 in = *reinterpret_cast<const uint4*>(codes + r * kHeadDim + 16 * q);
-      const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+      const uint32_t w[4] = {in[q].x, in[q].y, in[q].z, in[q].w};
       uint32_t out[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -634,22 +641,18 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
               page = 0;
             }
             const uint8_t* pg = reinterpret_cast<const uint8_t*>(a.pool) + (long long)page * a.page_bytes;
-            const long long rk = (long long)h * Ps + blk_so[pp];          // K row of the block
-            const long long rv = (long long)(H + h) * Ps + blk_so[pp];    // V row
-            const uint32_t code_bytes = (uint32_t)rows * kHeadDim;
-            const uint32_t dsts[4] = {smem_u32(&sm.f8.k[st8][pp * rows * kHeadDim]),
-                                      smem_u32(&sm.f8.v[st8][pp * rows * kHeadDim]),
-                                      smem_u32(&sm.f8.ke[st8][pp * rows]),
-                                      smem_u32(&sm.f8.ve[st8][pp * rows])};
-            const uint8_t* srcs[4] = {pg + rk * kHeadDim, pg + rv * kHeadDim, pg + a.exp_off + rk,
-                                      pg + a.exp_off + rv};
-            const uint32_t sizes[4] = {code_bytes, code_bytes, (uint32_t)rows, (uint32_t)rows};
+            const uint32_t blk_bytes = (uint32_t)rows * (kHeadDim + 1);
+            const uint32_t dsts[2] = {smem_u32(&sm.f8.k[st8][pp * blk_bytes]),
+                                      smem_u32(&sm.f8.v[st8][pp * blk_bytes])};
+            // blk_so is block-aligned, so the block starts at (plane row + blk_so) * 65
+            const long long kb = ((long long)h * Ps + blk_so[pp]) * (kHeadDim + 1);
+            const uint8_t* srcs[2] = {pg + kb, pg + kb + (long long)H * Ps * (kHeadDim + 1)};
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 2; ++c)
               asm volatile(
                   "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
                   "%2, [%3];\n" ::"r"(dsts[c]),
-                  "l"(srcs[c]), "r"(sizes[c]), "r"(mb)
+                  "l"(srcs[c]), "r"(blk_bytes), "r"(mb)
                   : "memory");
           }
         }
@@ -661,7 +664,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
         if (!mbar_wait(&sm.f8.full[st8], (j / kF8Stages) & 1, abort, a.err)) break;
         consumed = j + 1;
         if (!mbar_wait(&sm.kv_empty[s], ((j / kStages) & 1) ^ 1, abort, a.err)) break;
-        fp8_dequant_rows(sm.f8.k[st8], sm.f8.ke[st8], sm.k[s], sm.f8.nblk[st8] * rows, lane);
+        fp8_dequant_rows(sm.f8.k[st8], rows, sm.k[s], sm.f8.nblk[st8] * rows, lane);
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) {
@@ -975,7 +978,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
         const int st8 = j % kF8Stages, s = j % kStages;
         if (!mbar_wait(&sm.f8.full[st8], (j / kF8Stages) & 1, abort, a.err)) break;
         if (!mbar_wait(&sm.kv_empty[s], ((j / kStages) & 1) ^ 1, abort, a.err)) break;
-        fp8_dequant_rows(sm.f8.v[st8], sm.f8.ve[st8], sm.v[s], sm.f8.nblk[st8] * rows, lane);
+        fp8_dequant_rows(sm.f8.v[st8], rows, sm.v[s], sm.f8.nblk[st8] * rows, lane);
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) {

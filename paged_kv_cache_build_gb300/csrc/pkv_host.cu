@@ -61,7 +61,6 @@ struct pkv_ctx {
   long long page_elems = 0;      // bf16 elements per page (bf16 pools)
   int fp8 = 0;                   // 1: E4M3 pages with row exponents
   long long page_bytes = 0;      // bytes per page (either format)
-  long long exp_off = 0;         // FP8 pages: byte offset of the row exponents
   uint16_t* d_pool = nullptr;
   int32_t* d_free = nullptr;
   int* d_err = nullptr;
@@ -128,7 +127,6 @@ inline PoolView pool_view(pkv_t h, int layer) {
   pv.pool_pages = h->P;
   pv.fp8 = h->fp8;
   pv.page_bytes = h->page_bytes;
-  pv.exp_off = h->exp_off;
   pv.km_len = h->d_km_len ? h->d_km_len + (long long)layer * h->P : nullptr;
   return pv;
 }
@@ -281,7 +279,6 @@ static pkv_status create_cache(int pool_pages, int page_size, int heads, int hea
   h->fp8 = fp8;
   // FP8 pages: 64 code bytes and one exponent byte per row; bf16 pages: 128 bytes per row
   h->page_bytes = fp8 ? 2LL * heads * page_size * (head_dim + 1) : 2LL * h->page_elems;
-  h->exp_off = fp8 ? 2LL * heads * page_size * head_dim : 0;
   h->streams.resize(max_streams);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -753,7 +750,6 @@ static pkv_status window_reset(pkv_t h, Stream* st, cudaStream_t s) {
   ca.fp8 = h->fp8;
   ca.layer_bytes = (long long)h->P * h->page_bytes;
   ca.page_bytes = h->page_bytes;
-  ca.exp_off = h->exp_off;
   ca.layers = h->L;
   ca.heads = h->H;
   ca.page_size = h->Ps;
@@ -878,7 +874,6 @@ static pkv_status attend_args(pkv_t h, Stream* st, const void* q, int n_q, int l
   a->pool = layer_base(h, layer);
   a->page_elems = h->page_elems;
   a->page_bytes = h->page_bytes;
-  a->exp_off = h->exp_off;
   a->fp8 = h->fp8;
   a->page_size = h->Ps;
   a->pool_pages = h->P;
@@ -1377,12 +1372,22 @@ pkv_status pkv_read_page_fp8(pkv_t h, int layer, int page, int kv, void* codes_d
   if (layer < 0 || layer >= h->L || page < 0 || page >= h->P || (kv != 0 && kv != 1))
     return fail(h, PKV_ERR_INVALID, "layer/page/kv out of range");
   if (!h->fp8) return fail(h, PKV_ERR_INVALID, "this cache holds bf16 pages: use pkv_read_page");
-  const size_t rows = (size_t)h->H * h->Ps;
+  // the kv half of the page (heads planes of page_size rows, in 65-byte row
+  // blocks), then unpacked into [heads][page_size][64] codes and [heads][page_size]
+  // exponents
+  const size_t half = (size_t)h->H * h->Ps * (kHeadDim + 1);
+  std::vector<uint8_t> raw(half);
   PKV_CUDA(h, cudaDeviceSynchronize());
   const uint8_t* pg = reinterpret_cast<const uint8_t*>(layer_base(h, layer)) + (long long)page * h->page_bytes;
-  PKV_CUDA(h, cudaMemcpy(codes_dst, pg + (size_t)kv * rows * kHeadDim, rows * kHeadDim,
-                         cudaMemcpyDeviceToHost));
-  PKV_CUDA(h, cudaMemcpy(exps_dst, pg + h->exp_off + (size_t)kv * rows, rows, cudaMemcpyDeviceToHost));
+  PKV_CUDA(h, cudaMemcpy(raw.data(), pg + (size_t)kv * half, half, cudaMemcpyDeviceToHost));
+  uint8_t* codes = static_cast<uint8_t*>(codes_dst);
+  uint8_t* exps = static_cast<uint8_t*>(exps_dst);
+  for (int hh = 0; hh < h->H; ++hh)
+    for (int s = 0; s < h->Ps; ++s) {
+      const size_t row = (size_t)hh * h->Ps + s;
+      std::memcpy(codes + row * kHeadDim, raw.data() + fp8_code_off(h->H, h->Ps, 0, hh, s), kHeadDim);
+      exps[row] = raw[fp8_exp_off(h->H, h->Ps, 0, hh, s)];
+    }
   return PKV_OK;
 }
 

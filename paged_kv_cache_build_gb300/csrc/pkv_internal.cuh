@@ -29,9 +29,9 @@ __host__ __device__ __forceinline__ int swizzle_chunk(int slot, int chunk) {
 }
 
 // One layer's page set. bf16 pages: pool[page][kv][head][slot][64] bf16, rows
-// 128-byte swizzled. FP8 pages: per page the E4M3 codes [kv][head][slot][64]
-// (64-byte rows, unswizzled), then one exponent byte per row [kv][head][slot]
-// at exp_off: a row's values are decode(code) * 2^exponent.
+// 128-byte swizzled. FP8 pages: per page and (kv, head) plane, row blocks of
+// E4M3 codes (64-byte rows, unswizzled) each followed by its rows' exponent bytes
+// (fp8_code_off, fp8_exp_off below): a row's values are decode(code) * 2^exponent.
 struct PoolView {
   uint16_t* base;
   long long page_elems;   // bf16 pages: 2 * heads * page_size * 64
@@ -40,7 +40,6 @@ struct PoolView {
   int pool_pages;
   int fp8;                // 1: E4M3 pages
   long long page_bytes;   // bytes per page (either format)
-  long long exp_off;      // FP8 pages: byte offset of the exponents in a page
   int* km_len;            // bf16 pages: this layer's mean-key cache tags (per page), or null;
                           // a kernel that writes a page's rows sets its tag to -1
 };
@@ -68,15 +67,40 @@ __device__ __forceinline__ uint32_t fp8_pack2(float a, float b) {
   return r;
 }
 
+// FP8 page layout: for each (kv, head) plane of page_size rows, blocks of
+// B = min(page_size, 64) rows, each the B rows' 64 code bytes followed by their B
+// exponent bytes (B * 65 bytes, a multiple of 16), so that one bulk copy moves a
+// block's codes and exponents together. B is 16, 32 or 64 (page sizes are
+// multiples of 16 that divide or are divisible by 64).
+__host__ __device__ __forceinline__ int fp8_block_rows(int page_size) {
+  return page_size < 64 ? page_size : 64;
+}
+__host__ __device__ __forceinline__ long long fp8_block_off(int heads, int page_size, int kv,
+                                                            int head, int slot) {
+  const int B = fp8_block_rows(page_size);
+  return (long long)(kv * heads + head) * page_size * (kHeadDim + 1) +
+         (long long)(slot / B) * B * (kHeadDim + 1);
+}
+__host__ __device__ __forceinline__ long long fp8_code_off(int heads, int page_size, int kv, int head,
+                                                           int slot) {
+  return fp8_block_off(heads, page_size, kv, head, slot) +
+         (long long)(slot % fp8_block_rows(page_size)) * kHeadDim;
+}
+__host__ __device__ __forceinline__ long long fp8_exp_off(int heads, int page_size, int kv, int head,
+                                                          int slot) {
+  const int B = fp8_block_rows(page_size);
+  return fp8_block_off(heads, page_size, kv, head, slot) + (long long)B * kHeadDim + slot % B;
+}
+
 __device__ __forceinline__ uint8_t* fp8_row_codes(const PoolView& pv, int page, int kv, int head,
                                                   int slot) {
   return reinterpret_cast<uint8_t*>(pv.base) + (long long)page * pv.page_bytes +
-         ((long long)(kv * pv.heads + head) * pv.page_size + slot) * kHeadDim;
+         fp8_code_off(pv.heads, pv.page_size, kv, head, slot);
 }
 __device__ __forceinline__ int8_t* fp8_row_exp(const PoolView& pv, int page, int kv, int head,
                                                int slot) {
-  return reinterpret_cast<int8_t*>(pv.base) + (long long)page * pv.page_bytes + pv.exp_off +
-         (long long)(kv * pv.heads + head) * pv.page_size + slot;
+  return reinterpret_cast<int8_t*>(pv.base) + (long long)page * pv.page_bytes +
+         fp8_exp_off(pv.heads, pv.page_size, kv, head, slot);
 }
 
 // Stores 16-byte chunk c (values 8c .. 8c + 7) of row (page, kv, head, slot).
@@ -177,7 +201,7 @@ struct ResetCopyArgs {              // copy carried frames' special tokens, all 
   long long layer_elems;            // pool_pages * page_elems
   long long page_elems;
   int fp8;                          // E4M3 pages: rows are codes + an exponent byte
-  long long layer_bytes, page_bytes, exp_off;
+  long long layer_bytes, page_bytes;
   int layers, heads, page_size, pool_pages;
   int n_special, f_sp;
   const int32_t* special_list;      // old special list
@@ -289,7 +313,6 @@ struct AttendArgs {
   const uint16_t* pool;             // layer base
   long long page_elems;
   long long page_bytes;             // FP8 pages: bytes per page, and the exponents'
-  long long exp_off;                // byte offset inside a page
   int fp8;                          // 1: the pool holds E4M3 pages
   int page_size;
   int pool_pages;

@@ -243,9 +243,10 @@ __global__ void __launch_bounds__(256) reset_copy_kernel(const ResetCopyArgs a) 
         // FP8 pages: the row's codes (8 per chunk) and exponent move as they are
         const uint8_t* base = reinterpret_cast<const uint8_t*>(a.pool) + layer * a.layer_bytes +
                               (long long)src_page * a.page_bytes;
-        const long long row = (long long)(kv * H + h) * Ps + src_slot;
-        const uint2 codes = *reinterpret_cast<const uint2*>(base + row * kHeadDim + 8 * c);
-        val = make_uint4(codes.x, codes.y, c == 0 ? (uint32_t)(uint8_t)base[a.exp_off + row] : 0u, 0u);
+        const uint2 codes =
+            *reinterpret_cast<const uint2*>(base + fp8_code_off(H, Ps, kv, h, src_slot) + 8 * c);
+        val = make_uint4(codes.x, codes.y,
+                         c == 0 ? (uint32_t)base[fp8_exp_off(H, Ps, kv, h, src_slot)] : 0u, 0u);
       } else {
         const uint16_t* src = a.pool + layer * a.layer_elems + (long long)src_page * a.page_elems +
                               ((long long)(kv * H + h) * Ps + src_slot) * kHeadDim +
@@ -271,9 +272,9 @@ __global__ void __launch_bounds__(256) reset_copy_kernel(const ResetCopyArgs a) 
     if (a.fp8) {
       uint8_t* base = reinterpret_cast<uint8_t*>(a.pool) + layer * a.layer_bytes +
                       (long long)dst_page * a.page_bytes;
-      const long long row = (long long)(kv * H + h) * Ps + dst_slot;
-      *reinterpret_cast<uint2*>(base + row * kHeadDim + 8 * c) = make_uint2(val.x, val.y);
-      if (c == 0) base[a.exp_off + row] = (uint8_t)val.z;
+      *reinterpret_cast<uint2*>(base + fp8_code_off(H, Ps, kv, h, dst_slot) + 8 * c) =
+          make_uint2(val.x, val.y);
+      if (c == 0) base[fp8_exp_off(H, Ps, kv, h, dst_slot)] = (uint8_t)val.z;
       continue;
     }
     uint16_t* dst = a.pool + layer * a.layer_elems + (long long)dst_page * a.page_elems +
