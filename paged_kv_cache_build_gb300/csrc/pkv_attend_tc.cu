@@ -609,15 +609,17 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
       // stage kF8Stages tiles ahead; this warp dequantizes the K rows into the
       // operand ring (the second converting warp the V rows) and refills the
       // stage once both are done with it
+      // tiles are staged in order, so the table position (entry st_e, slot st_so)
+      // of the next block advances by one block each time (no division per tile)
+      int st_e = (int)((long long)t0 * kBN / Ps);
+      int st_so = (int)((long long)t0 * kBN - (long long)st_e * Ps);
       auto issue_stage = [&](int j) {
         const int st8 = j % kF8Stages;
-        const int tile = t0 + j;
         int nblk = 0, blk_page[kBN / 16], blk_so[kBN / 16];
 #pragma unroll
         for (int pp = 0; pp < kBN / 16; ++pp) {
           if (pp >= per) break;
-          const int f0 = tile * kBN + pp * rows;
-          const int e = f0 / Ps, so = f0 - e * Ps;
+          const int e = st_e, so = st_so;
           if (e >= a.n_entries) break;
           if ((e & ~31) != e_batch) {              // warp-uniform: next batch of entries
             e_batch = e & ~31;
@@ -627,6 +629,11 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
           blk_page[pp] = __shfl_sync(0xffffffffu, e_page, e - e_batch);
           blk_so[pp] = so;
           nblk = pp + 1;
+          st_so += rows;
+          if (st_so >= Ps) {
+            st_so = 0;
+            ++st_e;
+          }
         }
         if (lane == 0) {
           sm.f8.nblk[st8] = nblk;
