@@ -491,6 +491,50 @@ def extra_long24_full(fp8=False, frames=None, chunk=500, warm=80):
             "final_visible": {"pages": n_pages, "tokens": n_kv}}
 
 
+def extra_model24(frames=1000, warm=100, chunk=500):
+    """The model-shaped step, from native code (pkv_stream_model_frames): per frame,
+    for each of 24 layers, the frame's intra-frame attention, then the layer's
+    append and global attention over its visible pages; then evict (keyframe,
+    interval 4) or roll back. The 24-layer keyframe stream's shapes; frame
+    attention inputs are a second ring of 8 frames per layer. frame-steps/s and
+    p50 / p99 frame time over `frames` frames after `warm` frames."""
+    import torch
+    from paged_kv_cache_build_gb300 import PagedKVCache, frame_stream_cfg, synth_fill
+    from synth import TENSOR_K, TENSOR_Q, TENSOR_V, WORKLOADS, is_keyframe
+    w = WORKLOADS["long"]
+    L, R = w.layers, 8
+    cache = PagedKVCache(w.pool_pages, w.page_size, w.heads, w.head_dim, layers=L)
+    sid = cache.open_stream(frame_stream_cfg(w.num_scale, w.window, w.n_patch, w.n_special))
+    shape = (L, R, w.frame_tokens, w.heads, w.head_dim)
+    q, k, v, fq, fk, fv = (torch.empty(shape, dtype=torch.bfloat16, device="cuda") for _ in range(6))
+    out, fout = torch.empty_like(q), torch.empty_like(q)
+    for layer in range(L):
+        for t, (a, b_, c_) in enumerate(((q, k, v), (fq, fk, fv))):
+            synth_fill(a[layer], t, w.index, 0, layer, 0, TENSOR_Q, 0, w.q_scale)
+            synth_fill(b_[layer], t, w.index, 0, layer, 0, TENSOR_K)
+            synth_fill(c_[layer], t, w.index, 0, layer, 0, TENSOR_V)
+    F = warm + frames
+    keys = [is_keyframe(t, w.num_scale, w.keyframe_interval) for t in range(F)]
+    args = [list(x) for x in (fq, fk, fv, fout, q, k, v, out)]
+    cache.stream_model_frames(sid, *args, 0, warm, keys[:warm], sm_scale=w.sm_scale)
+    torch.cuda.synchronize()
+    per_frame, total_ms = [], 0.0
+    for f0 in range(warm, F, chunk):
+        n = min(chunk, F - f0)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        cache.stream_model_frames(sid, *args, f0, n, keys[f0:f0 + n], sm_scale=w.sm_scale, events=ev)
+        torch.cuda.synchronize()
+        per_frame += [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+        total_ms += ev[0].elapsed_time(ev[n])
+    cache.sync()
+    cache.close()
+    return {"workload": "model-24layer-kf4, frame + global attention per layer (frames %d-%d, "
+                        "native frame runs of %d)" % (warm, F - 1, chunk),
+            "frame_steps_per_s": round(frames / (total_ms * 1e-3), 2),
+            "ms_per_frame_step": round(total_ms / frames, 4),
+            "p50_ms": round(_percentile(per_frame, 0.5), 4), "p99_ms": round(_percentile(per_frame, 0.99), 4)}
+
+
 def extra_append(reps=20):
     """32 streams' frames appended in one batched launch (pkv_append_frames):
     2 x 262 x 16 x 64 x 2 B read and written per stream: GB/s against HBM."""
@@ -995,7 +1039,8 @@ def run_ours(args):
                          "long24": measured(extra_long24),
                          "append": measured(extra_append), "multistream": measured(extra_multistream),
                          "sampled": measured(extra_sampled), "frames": measured(extra_frames),
-                         "model24": measured(extra_long24, frame_attn=True),
+                         "model24": measured(extra_model24),
+                         "model24_eager": measured(extra_long24, frame_attn=True),
                          "blocksparse": measured(extra_blocksparse)}
     if not args.no_cpu_baseline and world == 1:      # the host baseline: N = 1 only
         line["cpu_baseline"] = oracle_sample(w, args.cpu_seconds)

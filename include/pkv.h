@@ -269,6 +269,29 @@ pkv_status pkv_stream_frames_multi(pkv_t h, int stream_id, int n_layers, const v
                                    void* const* out, float sm_scale, void* const* events,
                                    void* cuda_stream);
 
+/* The model-shaped step over the cache, driven from native code: VGGT's aggregator
+ * alternates each layer's frame attention (every frame's tokens over that frame's
+ * own tokens) with its global attention (vLLM-Omni RFC "Reconstruction Engine",
+ * sections 2.2 and 3.3); here the global attention is the cache's paged attention
+ * ("LingBot-Map Paged KV Cache", sections 2-3). For frame i and layer l it makes
+ * exactly these calls on cuda_stream:
+ *   pkv_attend_frames(h, fq[l] + slot, fk[l] + slot, fv[l] + slot, 1, tokens,
+ *                     fout[l] + slot, sm_scale)
+ *   pkv_append_frame(h, stream_id, l, k[l] + slot, v[l] + slot, tokens)
+ *   pkv_attend(h, q[l] + slot, tokens, stream_id, l, out[l] + slot, sm_scale)
+ * then, per frame, pkv_evict_window (keyframe == NULL or keyframe[i]) or
+ * pkv_rollback_last_frame, as pkv_stream_frames_multi. slot, the rings (fq, fk, fv,
+ * fout, q, k, v, out: HOST arrays of n_layers device pointers to bf16
+ * [ring][tokens][heads][64], each 16-byte aligned), keyframe and events are as in
+ * pkv_stream_frames_multi. Errors: as pkv_stream_frames_multi, and INVALID for a
+ * null or unaligned frame-attention pointer. */
+pkv_status pkv_stream_model_frames(pkv_t h, int stream_id, int n_layers, const void* const* fq,
+                                   const void* const* fk, const void* const* fv, void* const* fout,
+                                   const void* const* q, const void* const* k, const void* const* v,
+                                   void* const* out, int ring, int frame0, int n_frames, int tokens,
+                                   const unsigned char* keyframe, float sm_scale, void* const* events,
+                                   void* cuda_stream);
+
 /* Write the visible page table (section 2, build_visible_page_table): page ids in
  * the order scale -> window (oldest first) -> special (allocation order); chunked
  * mode: chunks oldest first, pages in order.

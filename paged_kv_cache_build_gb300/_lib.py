@@ -56,6 +56,12 @@ SIGNATURES = {
                                         ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p), c_int,
                                         c_int, c_int, c_int, c_void_p, ctypes.POINTER(c_void_p),
                                         c_float, ctypes.POINTER(c_void_p), c_void_p]),
+    "pkv_stream_model_frames": (c_int, [c_void_p, c_int, c_int, ctypes.POINTER(c_void_p),
+                                        ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p),
+                                        ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p),
+                                        ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p),
+                                        ctypes.POINTER(c_void_p), c_int, c_int, c_int, c_int,
+                                        c_void_p, c_float, ctypes.POINTER(c_void_p), c_void_p]),
     "pkv_sync": (c_int, [c_void_p, c_void_p]),
     "pkv_visible_count": (c_int, [c_void_p, c_int, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]),
     "pkv_free_pages": (c_int, [c_void_p, ctypes.POINTER(c_int)]),

@@ -243,6 +243,35 @@ class PagedKVCache:
             ctypes.cast(flags, ctypes.c_void_p) if flags else None, arr(outs, "out"), float(sm_scale),
             ev, _stream_ptr(stream)))
 
+    def stream_model_frames(self, sid, fqs, fks, fvs, fouts, qs, ks, vs, outs, frame0, n_frames,
+                            keyframe=None, sm_scale=0.0, events=None, stream=None):
+        """pkv_stream_model_frames: as stream_frames_multi, with each layer's
+        intra-frame attention (fqs/fks/fvs -> fouts, one ring per layer) before its
+        append and global attention."""
+        L = len(qs)
+        if not all(len(x) == L for x in (ks, vs, outs, fqs, fks, fvs, fouts)):
+            raise ValueError("one tensor of each kind per layer")
+        ring, tokens = qs[0].shape[0], qs[0].shape[1]
+        arr = lambda ts, name: (ctypes.c_void_p * L)(*[_bf16_ptr(t, name).value for t in ts])  # noqa: E731
+        flags = None
+        if keyframe is not None:
+            if len(keyframe) != n_frames:
+                raise ValueError("one keyframe flag per frame")
+            flags = (ctypes.c_ubyte * n_frames)(*[1 if f else 0 for f in keyframe])
+        ev = None
+        if events is not None:
+            if len(events) != n_frames + 1:
+                raise ValueError("n_frames + 1 events")
+            for e in events:
+                if not e.cuda_event:        # torch creates the CUDA event on its first record
+                    e.record(stream)
+            ev = (ctypes.c_void_p * (n_frames + 1))(*[e.cuda_event for e in events])
+        self._check(self.lib.pkv_stream_model_frames(
+            self.h, sid, L, arr(fqs, "fq"), arr(fks, "fk"), arr(fvs, "fv"), arr(fouts, "fout"),
+            arr(qs, "q"), arr(ks, "k"), arr(vs, "v"), arr(outs, "out"), ring, frame0, n_frames, tokens,
+            ctypes.cast(flags, ctypes.c_void_p) if flags else None, float(sm_scale), ev,
+            _stream_ptr(stream)))
+
     def attend_noalloc(self, q, sid, layer=0, out=None, sm_scale=0.0, stream=None):
         """pkv_attend_noalloc: attention whose scratch is a fixed device array."""
         if out is None:

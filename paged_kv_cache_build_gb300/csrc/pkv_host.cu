@@ -963,15 +963,19 @@ pkv_status pkv_stream_frames(pkv_t h, int sid, int layer, const void* q, const v
   return PKV_OK;
 }
 
-pkv_status pkv_stream_frames_multi(pkv_t h, int sid, int n_layers, const void* const* q,
-                                   const void* const* k, const void* const* v, int ring, int frame0,
-                                   int n_frames, int tokens, const unsigned char* keyframe,
-                                   void* const* out, float sm_scale, void* const* events,
-                                   void* cuda_stream) {
+// The native frame runner of pkv_stream_frames_multi and pkv_stream_model_frames:
+// per frame and layer, the frame's intra-frame attention (when fq is given), then
+// the layer's append and global attention; then the frame's evict or rollback.
+static pkv_status run_frames(pkv_t h, const char* fn, int sid, int n_layers, const void* const* q,
+                             const void* const* k, const void* const* v, const void* const* fq,
+                             const void* const* fk, const void* const* fv, void* const* fout,
+                             int ring, int frame0, int n_frames, int tokens,
+                             const unsigned char* keyframe, void* const* out, float sm_scale,
+                             void* const* events, void* cuda_stream) {
   Stream* st = nullptr;
   if (pkv_status r = get_stream(h, sid, &st)) return r;
   if (st->cfg.mode != PKV_MODE_FRAME)
-    return fail(h, PKV_ERR_STATE, "pkv_stream_frames_multi needs a frame-mode stream");
+    return fail(h, PKV_ERR_STATE, "%s needs a frame-mode stream", fn);
   if (st->pending) return fail(h, PKV_ERR_STATE, "a frame of stream %d is pending", sid);
   if (n_layers < 1 || n_layers > h->L)
     return fail(h, PKV_ERR_INVALID, "n_layers %d outside 1..%d", n_layers, h->L);
@@ -981,10 +985,17 @@ pkv_status pkv_stream_frames_multi(pkv_t h, int sid, int n_layers, const void* c
     return fail(h, PKV_ERR_INVALID, "tokens %d != n_patch + n_special", tokens);
   if (n_frames == 0) return PKV_OK;
   if (!q || !k || !v || !out) return fail(h, PKV_ERR_INVALID, "null pointer array");
-  for (int l = 0; l < n_layers; ++l)
+  const bool frame_attn = fq != nullptr;
+  if (frame_attn && (!fk || !fv || !fout)) return fail(h, PKV_ERR_INVALID, "null pointer array");
+  for (int l = 0; l < n_layers; ++l) {
     if (!q[l] || !k[l] || !v[l] || !out[l] || !aligned16(q[l]) || !aligned16(k[l]) ||
         !aligned16(v[l]) || !aligned16(out[l]))
       return fail(h, PKV_ERR_INVALID, "layer %d: q/k/v/out must be 16-byte aligned device pointers", l);
+    if (frame_attn && (!fq[l] || !fk[l] || !fv[l] || !fout[l] || !aligned16(fq[l]) ||
+                       !aligned16(fk[l]) || !aligned16(fv[l]) || !aligned16(fout[l])))
+      return fail(h, PKV_ERR_INVALID,
+                  "layer %d: frame-attention q/k/v/out must be 16-byte aligned device pointers", l);
+  }
   cudaStream_t s = as_stream(cuda_stream);
   const size_t fb = (size_t)tokens * h->H * kHeadDim * sizeof(uint16_t);   // bytes per frame
   for (int i = 0; i < n_frames; ++i) {
@@ -992,8 +1003,13 @@ pkv_status pkv_stream_frames_multi(pkv_t h, int sid, int n_layers, const void* c
     const size_t o = fb * (size_t)((frame0 + i) % ring);
     pkv_status r = PKV_OK;
     for (int l = 0; l < n_layers && r == PKV_OK; ++l) {
-      r = pkv_append_frame(h, sid, l, static_cast<const char*>(k[l]) + o,
-                           static_cast<const char*>(v[l]) + o, tokens, cuda_stream);
+      if (frame_attn)
+        r = pkv_attend_frames(h, static_cast<const char*>(fq[l]) + o, static_cast<const char*>(fk[l]) + o,
+                              static_cast<const char*>(fv[l]) + o, 1, tokens,
+                              static_cast<char*>(fout[l]) + o, sm_scale, cuda_stream);
+      if (r == PKV_OK)
+        r = pkv_append_frame(h, sid, l, static_cast<const char*>(k[l]) + o,
+                             static_cast<const char*>(v[l]) + o, tokens, cuda_stream);
       if (r == PKV_OK)
         r = pkv_attend(h, static_cast<const char*>(q[l]) + o, tokens, sid, l,
                        static_cast<char*>(out[l]) + o, sm_scale, cuda_stream);
@@ -1009,6 +1025,27 @@ pkv_status pkv_stream_frames_multi(pkv_t h, int sid, int n_layers, const void* c
   if (events && events[n_frames])
     PKV_CUDA(h, cudaEventRecord(static_cast<cudaEvent_t>(events[n_frames]), s));
   return PKV_OK;
+}
+
+pkv_status pkv_stream_frames_multi(pkv_t h, int sid, int n_layers, const void* const* q,
+                                   const void* const* k, const void* const* v, int ring, int frame0,
+                                   int n_frames, int tokens, const unsigned char* keyframe,
+                                   void* const* out, float sm_scale, void* const* events,
+                                   void* cuda_stream) {
+  return run_frames(h, "pkv_stream_frames_multi", sid, n_layers, q, k, v, nullptr, nullptr, nullptr,
+                    nullptr, ring, frame0, n_frames, tokens, keyframe, out, sm_scale, events,
+                    cuda_stream);
+}
+
+pkv_status pkv_stream_model_frames(pkv_t h, int sid, int n_layers, const void* const* fq,
+                                   const void* const* fk, const void* const* fv, void* const* fout,
+                                   const void* const* q, const void* const* k, const void* const* v,
+                                   void* const* out, int ring, int frame0, int n_frames, int tokens,
+                                   const unsigned char* keyframe, float sm_scale, void* const* events,
+                                   void* cuda_stream) {
+  if (!fq || !fk || !fv || !fout) return fail(h, PKV_ERR_INVALID, "null pointer array");
+  return run_frames(h, "pkv_stream_model_frames", sid, n_layers, q, k, v, fq, fk, fv, fout, ring,
+                    frame0, n_frames, tokens, keyframe, out, sm_scale, events, cuda_stream);
 }
 
 pkv_status pkv_attend_chunked(pkv_t h, const void* q, int n_q, int sid, int layer, void* out,

@@ -150,3 +150,52 @@ def test_multi_layer_run_equals_separate_calls(fp8):
     for c in caches:
         c.sync()
         c.close()
+
+
+def test_model_run_equals_separate_calls():
+    """pkv_stream_model_frames: 3 layers, a ring of 5 input frames, keyframe
+    interval 4; each layer's frame attention, append and global attention equal
+    the same calls made one by one, outputs bit for bit and the cache state."""
+    from paged_kv_cache_build_gb300 import PagedKVCache, frame_stream_cfg, synth_fill
+    w = WORKLOADS["long"]
+    L, R, frames = 3, 5, 30
+    shape = (L, R, w.frame_tokens, w.heads, w.head_dim)
+    q, k, v, fq, fk, fv = (torch.empty(shape, dtype=torch.bfloat16, device="cuda") for _ in range(6))
+    for layer in range(L):
+        synth_fill(q[layer], 2, w.index, 0, layer, 0, TENSOR_Q, 0, w.q_scale)
+        synth_fill(k[layer], 2, w.index, 0, layer, 0, TENSOR_K)
+        synth_fill(v[layer], 2, w.index, 0, layer, 0, TENSOR_V)
+        synth_fill(fq[layer], 3, w.index, 0, layer, 0, TENSOR_Q, 0, w.q_scale)
+        synth_fill(fk[layer], 3, w.index, 0, layer, 0, TENSOR_K)
+        synth_fill(fv[layer], 3, w.index, 0, layer, 0, TENSOR_V)
+    caches = [PagedKVCache(w.pool_pages, w.page_size, w.heads, w.head_dim, layers=L) for _ in range(2)]
+    sids = [c.open_stream(frame_stream_cfg(w.num_scale, w.window, w.n_patch, w.n_special))
+            for c in caches]
+    keys = [is_keyframe(t, w.num_scale, 4) for t in range(frames)]
+    out_a, fout_a = torch.zeros_like(q), torch.zeros_like(q)
+    out_b, fout_b = torch.zeros_like(q), torch.zeros_like(q)
+    caches[0].stream_model_frames(sids[0], list(fq), list(fk), list(fv), list(fout_a), list(q), list(k),
+                                  list(v), list(out_a), 0, frames, keys, sm_scale=w.sm_scale)
+    b, sb = caches[1], sids[1]
+    for t in range(frames):
+        for layer in range(L):
+            b.attend_frames(fq[layer, t % R], fk[layer, t % R], fv[layer, t % R],
+                            out=fout_b[layer, t % R], sm_scale=w.sm_scale)
+            b.append_frame(sb, k[layer, t % R], v[layer, t % R], layer)
+            b.attend(q[layer, t % R], sb, layer, out=out_b[layer, t % R], sm_scale=w.sm_scale)
+        if keys[t]:
+            b.evict_window(sb)
+        else:
+            b.rollback_last_frame(sb)
+    torch.cuda.synchronize()
+    for got, want in ((out_a, out_b), (fout_a, fout_b)):
+        np.testing.assert_array_equal(got.view(torch.int16).cpu().numpy(), want.view(torch.int16).cpu().numpy())
+    assert _state(caches[0], sids[0]) == _state(b, sb)
+    from paged_kv_cache_build_gb300._lib import STATUS_NAMES
+    status = caches[0].lib.pkv_stream_model_frames(caches[0].h, sids[0], L, None, None, None, None,
+                                                   None, None, None, None, R, frames, 1, w.frame_tokens,
+                                                   None, 0.0, None, None)
+    assert STATUS_NAMES.get(status) == "INVALID"                 # null frame-attention rings
+    for c in caches:
+        c.sync()
+        c.close()
