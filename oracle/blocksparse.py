@@ -14,9 +14,12 @@ The estimate decides which pages are kept, so it is defined to the bit, in IEEE
 fp32 (the precision of the kernel that makes the same decision):
     qm[h][d] = (sum over query rows i = 0, 1, ... of q[i][h][d]) / n_q
     km[h][d] = (sum over the page's valid slots s = 0, 1, ... of K[s][h][d]) / len
-    score    = sum over h = 0, 1, ..., then d = 0, 1, ..., of (qm[h][d] * km[h][d])
+    s_h      = sum over d = 0, 1, ... of (qm[h][d] * km[h][d])      (each head h)
+    score    = sum over h = 0, 1, ... of s_h
 every sum a running fp32 total that starts at 0, every product and quotient
-rounded once (no fused multiply-add).
+rounded once (no fused multiply-add). The pages fix no order; this one (a sum per
+head, then over the heads) is the reading taken because its per-head sums are
+independent, so a kernel forms them at once.
 """
 
 import math
@@ -39,12 +42,15 @@ def pooled_mean(rows_bits):
 
 
 def page_score(qm, km):
-    """The estimate: a running fp32 sum over (h, d) in order of fp32 products."""
+    """The estimate: per head, a running fp32 sum over d in order of the fp32
+    products; then a running fp32 sum of the heads' sums in head order."""
     acc = np.float32(0.0)
     H, D = qm.shape
     for h in range(H):
+        s_h = np.float32(0.0)
         for d in range(D):
-            acc = np.float32(acc + np.float32(qm[h, d] * km[h, d]))
+            s_h = np.float32(s_h + np.float32(qm[h, d] * km[h, d]))
+        acc = np.float32(acc + s_h)
     return acc
 
 

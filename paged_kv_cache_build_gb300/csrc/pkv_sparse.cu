@@ -13,7 +13,8 @@
 // one fixed fp32 order with every operation rounded once:
 //   qm[h][d] = (sum over rows i in order of q[i][h][d]) / n_q
 //   km[h][d] = (sum over valid slots s in order of K[s][h][d]) / len
-//   score    = sum over h, then d, in order of (qm[h][d] * km[h][d])
+//   s_h      = sum over d in order of (qm[h][d] * km[h][d])   (each head h)
+//   score    = sum over h in order of s_h
 // (__fadd_rn / __fmul_rn / __fdiv_rn: no contraction into fused multiply-adds).
 // A page's km depends only on its rows, so each layer keeps a cache of km per
 // page, tagged with the valid length it was computed at; the append and the
@@ -111,7 +112,8 @@ __device__ void select_kept(const PageScoreArgs& a) {
 }
 
 // Score of page e (block e): the products qm * km of its cached mean keys (all
-// threads), added in (h, d) order as one running sum (one thread); the page's
+// threads), each head's added over d in order (one thread per head), then the
+// heads' sums in head order (one thread); the page's
 // tag becomes its valid length (every stale km was recomputed by the launch
 // before). A recomputed km is the same fp32 value as a cached one, bit for bit
 // (same operations, same order), and every kernel that writes a page's rows sets
@@ -123,6 +125,7 @@ __global__ void __launch_bounds__(256) page_score_kernel(const PageScoreArgs a) 
   pdl_wait();
   pdl_trigger();
   __shared__ __align__(16) float prod[kMaxHeads * kHeadDim];
+  __shared__ float head_sum[kMaxHeads];
   __shared__ int s_last;
   const int e = blockIdx.x, n = a.heads * kHeadDim;   // n: a multiple of 64
   int page = 0, len = 0;
@@ -135,20 +138,26 @@ __global__ void __launch_bounds__(256) page_score_kernel(const PageScoreArgs a) 
       prod[i] = __fmul_rn(__ldcg(a.qm + i), __ldcg(cache + i));
   }
   __syncthreads();
+  if (ok && threadIdx.x < a.heads) {
+    const float4* p4 = reinterpret_cast<const float4*>(prod + threadIdx.x * kHeadDim);
+    float s_h = 0.f;
+#pragma unroll
+    for (int i = 0; i < kHeadDim / 4; ++i) {
+      const float4 v = p4[i];
+      s_h = __fadd_rn(s_h, v.x);
+      s_h = __fadd_rn(s_h, v.y);
+      s_h = __fadd_rn(s_h, v.z);
+      s_h = __fadd_rn(s_h, v.w);
+    }
+    head_sum[threadIdx.x] = s_h;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     float acc = __int_as_float(0x7fc00000);               // NaN: ranks lowest
     if (ok) {
       a.km_len[page] = len;
-      const float4* p4 = reinterpret_cast<const float4*>(prod);
       acc = 0.f;
-#pragma unroll 8
-      for (int i = 0; i < n / 4; ++i) {
-        const float4 v = p4[i];
-        acc = __fadd_rn(acc, v.x);
-        acc = __fadd_rn(acc, v.y);
-        acc = __fadd_rn(acc, v.z);
-        acc = __fadd_rn(acc, v.w);
-      }
+      for (int hh = 0; hh < a.heads; ++hh) acc = __fadd_rn(acc, head_sum[hh]);
     } else {
       atomicOr(a.err, kErrPageRange);
     }

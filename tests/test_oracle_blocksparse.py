@@ -40,6 +40,16 @@ def test_score_order_is_sequential_fp32():
     assert page_score(np.array([[a]], np.float32), np.array([[a]], np.float32)) == np.float32(a * a)
 
 
+def test_score_sums_each_head_first():
+    """The heads' sums are formed first, then added in head order: with head 0's
+    products (1e8, 0) and head 1's (-1e8, 1), head 1's sum is -1e8 (the 1 is
+    absorbed: fp32 spacing at 1e8 is 8), so the score is 1e8 + (-1e8) = 0; one
+    running sum over all products in order would give 1e8 + 0 - 1e8 + 1 = 1."""
+    qm = np.array([[1e8, 0.0], [-1e8, 1.0]], dtype=np.float32)
+    km = np.ones((2, 2), dtype=np.float32)
+    assert page_score(qm, km) == np.float32(0.0)
+
+
 def test_ranking_rule_brute_force():
     rng = np.random.default_rng(1)
     for trial in range(200):
