@@ -448,11 +448,14 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
   const uint16_t* const qg = a.q + row_base * H * kHeadDim;
   uint16_t* const og = a.out + row_base * H * kHeadDim;
 
+  // The KV split varies fastest, so the splits of one (head, M-group) run in the
+  // same wave and its query tile is fetched from DRAM once; the M-groups of a
+  // head come next, so they share that head's pages through L2.
   int bid = cw.bid;
+  const int split = bid % a.num_splits;
+  bid /= a.num_splits;
   const int mg = bid % n_mgroups;
-  bid /= n_mgroups;
-  const int h = bid % H;
-  const int split = bid / H;
+  const int h = bid / n_mgroups;
   const int t0 = (int)((long long)n_tiles * split / a.num_splits);
   const int t1 = (int)((long long)n_tiles * (split + 1) / a.num_splits);
   const int nT = t1 - t0;
