@@ -77,22 +77,29 @@ constexpr float kSumLimit = 18446744073709551616.0f;   // 2^64
 
 // FP8 pages: the producer bulk-copies a tile's E4M3 codes and row exponents into
 // a staging ring, one copy per row block of K and of V (the page's layout: B rows
-// of 64 code bytes, then their B exponents); two warps dequantize them into the
-// bf16 operand ring.
+// of 64 code bytes, then their B exponents), and warps dequantize them into the
+// bf16 operand ring. Without extra rows the producer converts the K rows and one
+// more warp the V rows. With extra rows the producer only stages, and four warps
+// (three extra-row warps and one more, one per SM sub-partition) each convert the
+// K and V rows of one 16-slot quarter of the tile, one row per lane; the extra-row
+// warps convert three tiles ahead of the tile they work on.
 constexpr int kF8Stages = 4;
+template <bool EXTRA>
+constexpr int kF8Deq = EXTRA ? 4 : 2;      // dequantizing warps (arrivals per stage)
 template <bool FP8>
 struct __align__(128) F8Ring {
   alignas(128) uint8_t k[kF8Stages][kBN * (kHeadDim + 1)];   // K row blocks, as in the page
   alignas(128) uint8_t v[kF8Stages][kBN * (kHeadDim + 1)];
   int nblk[kF8Stages];                     // page blocks copied into the stage
   uint64_t full[kF8Stages];                // the stage's copies have landed
-  uint64_t free_[kF8Stages];               // both converting warps are done with it
+  uint64_t free_[kF8Stages];               // every dequantizing warp is done with it
 };
 template <>
 struct F8Ring<false> {
   uint64_t unused;
 };
 static_assert(sizeof(F8Ring<true>) % 128 == 0, "staging ring alignment");
+
 
 template <int MT, bool FP8 = false>
 struct __align__(1024) TcSmem {
@@ -330,7 +337,7 @@ __device__ __forceinline__ uint32_t sw_addr(uint32_t base, int r, int c) {
 
 // Warps: 0 extra rows, 1 MMA issuer (M-tile 1), 2 producer, 3 MMA issuer
 // (M-tile 0), 4 .. 4 + 4 MT - 1 softmax, then kXWarps - 1 more extra-row warps,
-// then (FP8 pages) the second dequantizing warp.
+// then (FP8 pages) one more dequantizing warp.
 template <int MT, bool EXTRA, bool FP8 = false>
 __host__ __device__ constexpr int tc_threads() {
   return (4 + 4 * MT + (EXTRA ? kXWarps - 1 : 0) + (FP8 ? 1 : 0)) * 32;
@@ -389,46 +396,80 @@ __device__ __forceinline__ uint64_t tile_mask(const AttendArgs& a, const uint16_
   return bits;
 }
 
-// Dequantizes `rows` 64-value rows of FP8 codes from a staging stage (row blocks
-// of B rows: the B rows' 64 code bytes, then their B exponents) into a bf16
-// operand tile at its 128-byte-swizzled place, two rows per lane of one warp (row
-// lane, lane + 32). A row's 64 codes are loaded before any is converted.
-// decode(code) is exact in f16, f16 -> fp32 is exact, and the power-of-two scale
-// and the final bf16 rounding are exact for these values (at most 4 significant
-// bits).
-__device__ __forceinline__ void fp8_dequant_rows(const uint8_t* stage, int B, uint8_t* dst, int rows,
-                                                 int lane) {
-  for (int r = lane; r < rows; r += 32) {
-    const uint8_t* blk = stage + (r / B) * B * (kHeadDim + 1);
-    const int rb = r % B;
-    const float sc =
-        __uint_as_float((uint32_t)(127 + (int8_t)blk[B * kHeadDim + rb]) << 23);   // 2^e, |e| <= 126
-    uint4 in[4];
+// FP8 pages are staged as row blocks of B rows: the B rows' 64 code bytes, then
+// their B exponents. decode(code) is exact in f16, f16 -> fp32 is exact, and the
+// power-of-two scale and the final bf16 rounding are exact for these values (at
+// most 4 significant bits).
+__device__ __forceinline__ float fp8_row_scale(const uint8_t* blk, int B, int rb) {
+  return __uint_as_float((uint32_t)(127 + (int8_t)blk[B * kHeadDim + rb]) << 23);   // 2^e, |e| <= 126
+}
+// 16 codes -> 16 bf16 (8 pairs)
+__device__ __forceinline__ void fp8_convert16(uint4 in, float sc, uint32_t out[8]) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) in[q] = *reinterpret_cast<const uint4*>(blk + rb * kHeadDim + 16 * q);
+  for (int i = 0; i < 4; ++i) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t w[4] = {in[q].x, in[q].y, in[q].z, in[q].w};
-      uint32_t out[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int hw = 0; hw < 2; ++hw) {
-          const uint16_t pair = (uint16_t)(w[i] >> (16 * hw));
-          uint32_t h2;
-          asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(h2) : "h"(pair));
-          const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * sc;
-          const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16))) * sc;
-          out[2 * i + hw] = pack_bf16(lo, hi);
-        }
-      }
-      uint8_t* row = dst + r * 128;
-      *reinterpret_cast<uint4*>(row + (swizzle_chunk(r, 2 * q) << 4)) =
-          make_uint4(out[0], out[1], out[2], out[3]);
-      *reinterpret_cast<uint4*>(row + (swizzle_chunk(r, 2 * q + 1) << 4)) =
-          make_uint4(out[4], out[5], out[6], out[7]);
+    for (int hw = 0; hw < 2; ++hw) {
+      const uint16_t pair = (uint16_t)(w[i] >> (16 * hw));
+      uint32_t h2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(h2) : "h"(pair));
+      const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * sc;
+      const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16))) * sc;
+      out[2 * i + hw] = pack_bf16(lo, hi);
     }
   }
+}
+// values 16 q .. 16 q + 15 of row r, into their two 16-byte chunks of the
+// 128-byte-swizzled bf16 row
+__device__ __forceinline__ void fp8_store16(uint8_t* dst, int r, int q, const uint32_t out[8]) {
+  uint8_t* row = dst + r * 128;
+  *reinterpret_cast<uint4*>(row + (swizzle_chunk(r, 2 * q) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+  *reinterpret_cast<uint4*>(row + (swizzle_chunk(r, 2 * q + 1) << 4)) =
+      make_uint4(out[4], out[5], out[6], out[7]);
+}
+// row r (64 values); the row's 64 codes are loaded before any is converted. One
+// out-of-line copy serves every converting warp, which keeps the kernel's
+// instruction footprint small.
+__device__ __noinline__ void fp8_dequant_row(const uint8_t* stage, int B, uint8_t* dst, int r) {
+  const uint8_t* blk = stage + (r / B) * B * (kHeadDim + 1);
+  const int rb = r % B;
+  const float sc = fp8_row_scale(blk, B, rb);
+  uint4 in[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) in[q] = *reinterpret_cast<const uint4*>(blk + rb * kHeadDim + 16 * q);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t out[8];
+    fp8_convert16(in[q], sc, out);
+    fp8_store16(dst, r, q, out);
+  }
+}
+// `rows` rows of one operand (K or V), two per lane of one warp (row lane, lane + 32).
+__device__ __forceinline__ void fp8_dequant_rows(const uint8_t* stage, int B, uint8_t* dst, int rows,
+                                                 int lane) {
+  for (int r = lane; r < rows; r += 32) fp8_dequant_row(stage, B, dst, r);
+}
+
+// One tile's share of a quarter-converting warp (FP8 pages with extra rows):
+// once the stage's codes have landed and the operand stage is free, the K rows
+// (lanes 0-15) and the V rows (lanes 16-31) of slots 16 dq .. 16 dq + 15, then
+// the warp's arrivals on the operand stage and on the staging stage.
+template <int MT>
+__device__ __forceinline__ bool fp8_dequant_quarter(TcSmem<MT, true>& sm, int j, int dq, int B,
+                                                    int lane, volatile int* abort, int* err) {
+  const int st8 = j % kF8Stages, s = j % kStages;
+  if (!mbar_wait(&sm.f8.full[st8], (j / kF8Stages) & 1, abort, err)) return false;
+  if (!mbar_wait(&sm.kv_empty[s], ((j / kStages) & 1) ^ 1, abort, err)) return false;
+  const int r = 16 * dq + (lane & 15);
+  if (r < sm.f8.nblk[st8] * B)
+    fp8_dequant_row(lane < 16 ? sm.f8.k[st8] : sm.f8.v[st8], B, lane < 16 ? sm.k[s] : sm.v[s], r);
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0) {
+    mbar_arrive(&sm.kv_full[s]);
+    mbar_arrive(&sm.f8.free_[st8]);
+  }
+  return true;
 }
 
 template <int MT, bool EXTRA, bool FP8, typename Params>
@@ -464,13 +505,13 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
   // ---- set-up: barriers, zeroed KV ring, Q tiles, TMEM
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.kv_full[s], FP8 ? 2 : 1);          // copy (tx) or the two dequantizers
+      mbar_init(&sm.kv_full[s], FP8 ? kF8Deq<EXTRA> : 1);   // copy (tx) or the dequantizers
       mbar_init(&sm.kv_empty[s], MT + (EXTRA ? kXWarps : 0));   // M-tiles (softmax), extra warps
     }
     if constexpr (FP8) {
       for (int s = 0; s < kF8Stages; ++s) {
         mbar_init(&sm.f8.full[s], 1);
-        mbar_init(&sm.f8.free_[s], 2);
+        mbar_init(&sm.f8.free_[s], kF8Deq<EXTRA>);
       }
     }
     for (int m = 0; m < MT; ++m) {
@@ -609,9 +650,9 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
     const int rows = Ps >= kBN ? kBN : Ps;         // slots per block
     if constexpr (FP8 && !kDense) {
       // FP8 pages: each tile's codes and row exponents are copied into a staging
-      // stage kF8Stages tiles ahead; this warp dequantizes the K rows into the
-      // operand ring (the second converting warp the V rows) and refills the
-      // stage once both are done with it
+      // stage kF8Stages tiles ahead. Without extra rows this warp dequantizes the
+      // K rows into the operand ring (one more warp the V rows) and refills the
+      // stage once both are done with it; with extra rows it only stages
       // tiles are staged in order, so the table position (entry st_e, slot st_so)
       // of the next block advances by one block each time (no division per tile)
       int st_e = (int)((long long)t0 * kBN / Ps);
@@ -669,7 +710,18 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
       };
       int issued = 0, consumed = 0;
       for (; issued < nT && issued < kF8Stages; ++issued) issue_stage(issued);
-      for (int j = 0; j < nT; ++j) {
+      if constexpr (EXTRA) {
+        // staging only: a stage is refilled once the four quarter warps are done
+        // with its previous tile
+        for (; issued < nT; ++issued) {
+          if (!mbar_wait(&sm.f8.free_[issued % kF8Stages], (issued / kF8Stages - 1) & 1, abort,
+                         a.err))
+            break;
+          issue_stage(issued);
+        }
+        consumed = issued > kF8Stages ? issued - kF8Stages : 0;
+      }
+      for (int j = 0; !EXTRA && j < nT; ++j) {
         const int st8 = j % kF8Stages, s = j % kStages;
         if (!mbar_wait(&sm.f8.full[st8], (j / kF8Stages) & 1, abort, a.err)) break;
         consumed = j + 1;
@@ -981,10 +1033,13 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
     if (write && a.num_splits > 1)
       *reinterpret_cast<float2*>(a.part_ml + ro * 2) = make_float2(m_run, l_run);
   } else if (FP8 && !kDense && warp == tc_conv_warp<MT, EXTRA>()) {
-    // ===================================================== V dequantizer (FP8)
+    // ============================ V dequantizer, or the fourth quarter warp (FP8)
     if constexpr (FP8 && !kDense) {
       const int rows = Ps >= kBN ? kBN : Ps;
-      for (int j = 0; j < nT; ++j) {
+      if constexpr (EXTRA)
+        for (int j = 0; j < nT; ++j)
+          if (!fp8_dequant_quarter<MT>(sm, j, kF8Deq<EXTRA> - 1, rows, lane, abort, a.err)) break;
+      for (int j = 0; !EXTRA && j < nT; ++j) {
         const int st8 = j % kF8Stages, s = j % kStages;
         if (!mbar_wait(&sm.f8.full[st8], (j / kF8Stages) & 1, abort, a.err)) break;
         if (!mbar_wait(&sm.kv_empty[s], ((j / kStages) & 1) ^ 1, abort, a.err)) break;
@@ -1007,6 +1062,9 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
     // movmatrix. Softmax runs over slots, i.e. across the 8 lanes that share a
     // query column.
     const int xi = warp == kXWarp ? 0 : warp - (4 + 4 * MT) + 1;
+    // FP8 pages: warps 1..3 convert quarter xi - 1 of every tile, kF8Ahead tiles ahead
+    constexpr int kF8Ahead = 3;
+    const int dq = xi - 1;
     const int xr0 = row0 + MT * 128;               // first extra row
     const int g = lane >> 2, tq = lane & 3;
     // B fragments of Q_x^T: (k = d 2tq.., n = query g)
@@ -1029,8 +1087,18 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
     for (int i = 0; i < 4; ++i) ox[i][0] = ox[i][1] = ox[i][2] = ox[i][3] = 0.f;
     const float sl2 = a.scale_log2;
     bool alive = true;
-    for (int j = 0; j < nT; ++j) {
+    if constexpr (FP8 && !kDense)
+      for (int jj = 0; dq >= 0 && alive && jj < kF8Ahead && jj < nT; ++jj)
+        alive = fp8_dequant_quarter<MT>(sm, jj, dq, Ps >= kBN ? kBN : Ps, lane, abort, a.err);
+    for (int j = 0; alive && j < nT; ++j) {
       const int st = j % kStages;
+      if constexpr (FP8 && !kDense) {
+        if (dq >= 0 && j + kF8Ahead < nT &&
+            !fp8_dequant_quarter<MT>(sm, j + kF8Ahead, dq, Ps >= kBN ? kBN : Ps, lane, abort, a.err)) {
+          alive = false;
+          break;
+        }
+      }
       if (!mbar_wait(&sm.kv_full[st], (j / kStages) & 1, abort, a.err)) {
         alive = false;
         break;
