@@ -122,6 +122,29 @@ def test_fp8_random_streams_with_windowed_resets(seed):
     pr.gpu.sync()
 
 
+@pytest.mark.parametrize("ps", [16, 32])
+def test_fp8_extra_rows_with_small_pages(ps):
+    """Chunks of 2 frames of 131 tokens, i.e. 262 queries (two M-tiles plus extra
+    rows, whose warps dequantize quarters of every tile), on FP8 pages of 16 and
+    32 slots, so that a 64-slot tile spans four or two page blocks; 3 chunks
+    visible, every row of every chunk."""
+    w = WORKLOADS["chunked"].with_(page_size=ps, chunk_size=2, tokens_per_frame=131, sliding_window_num=3,
+                                   heads=2, frames=10)
+    pr = Pair(w, seed=5, fp8=True, pool_pages=128)
+    sid = pr.open()
+    for c in range(5):
+        frames = [2 * c, 2 * c + 1]
+        for f in frames:
+            pr.append(sid, f)
+        pr.check_meta(sid)
+        out = pr.gpu.attend_chunked(pr.gpu_q_chunk(sid, 0, frames), sid, 0, sm_scale=w.sm_scale)
+        o, e = pr.oracle_attention(sid, 0, pr.cpu_q(sid, 0, frames))
+        assert_close(out, o, e, f"fp8 page {ps} chunk {c}")
+        pr.evict(sid)
+    pr.check_pool(sid)
+    pr.gpu.sync()
+
+
 def test_fp8_chunked_stream():
     """Chunked sliding-window attention on FP8 pages: chunks of 4 frames of 300
     tokens, 3 visible, 4 heads; every row of every chunk."""
