@@ -55,7 +55,8 @@ constexpr int kBN = kTileSlots;    // slots per KV tile (64)
 constexpr int kMaxMaskTiles = 512; // tiles of a CTA whose slot masks are precomputed
 constexpr int kStages = 8;         // KV ring depth
 constexpr int kXRows = 8;          // extra query rows handled with mma.sync
-constexpr int kXWarps = kBN / 16;  // extra-row warps: one 16-slot quarter of a tile each
+constexpr int kXWarps = 4;         // extra-row warps: every fourth tile each
+static_assert(kStages % kXWarps == 0, "a stage's tiles belong to one extra-row warp");
 // S buffers per M-tile: tile j uses buffer j % kSBufs, and P of the tile (bf16
 // pairs) is written over the first 32 columns of its own S buffer.
 constexpr int kSBufs = 3;
@@ -506,7 +507,7 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.kv_full[s], FP8 ? kF8Deq<EXTRA> : 1);   // copy (tx) or the dequantizers
-      mbar_init(&sm.kv_empty[s], MT + (EXTRA ? kXWarps : 0));   // M-tiles (softmax), extra warps
+      mbar_init(&sm.kv_empty[s], MT + (EXTRA ? 1 : 0));   // M-tiles (softmax), the tile's extra-row warp
     }
     if constexpr (FP8) {
       for (int s = 0; s < kF8Stages; ++s) {
@@ -1054,9 +1055,12 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
     }
   } else if (EXTRA && (warp == kXWarp || (warp >= 4 + 4 * MT && warp < tc_conv_warp<MT, EXTRA>()))) {
     // ============================================== extra rows (mma.sync, regs)
-    // Up to 8 query rows, shared by kXWarps warps: warp xi takes slots 16 xi ..
-    // 16 xi + 15 of every tile with its own running max, sum and O, and the
-    // partial results are merged at the end. Transposed so that the 8 queries
+    // Up to 8 query rows, shared by kXWarps warps: warp xi takes every kXWarps-th
+    // tile (tiles xi, xi + kXWarps, ...; all 64 slots, so the four slot groups'
+    // MMAs are independent and the softmax bookkeeping is paid once a tile) with
+    // its own running max, sum and O, and the partial results are merged at the
+    // end. A stage's tiles are kStages apart, a multiple of kXWarps, so each stage
+    // is always released by the same warp. Transposed so that the 8 queries
     // are the N = 8 side of m16n8k16 tiles and the slots the M = 16 side:
     // S^T = K Q_x^T, then O^T += V^T P^T with P^T moved into B fragments by
     // movmatrix. Softmax runs over slots, i.e. across the 8 lanes that share a
@@ -1090,38 +1094,46 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
     if constexpr (FP8 && !kDense)
       for (int jj = 0; dq >= 0 && alive && jj < kF8Ahead && jj < nT; ++jj)
         alive = fp8_dequant_quarter<MT>(sm, jj, dq, Ps >= kBN ? kBN : Ps, lane, abort, a.err);
-    for (int j = 0; alive && j < nT; ++j) {
-      const int st = j % kStages;
+    // tiles xi, xi + kXWarps, ...: all 64 slots of each (four 16-slot groups)
+    for (int j = FP8 && !kDense ? 0 : xi; alive && j < nT; j += FP8 && !kDense ? 1 : kXWarps) {
       if constexpr (FP8 && !kDense) {
         if (dq >= 0 && j + kF8Ahead < nT &&
             !fp8_dequant_quarter<MT>(sm, j + kF8Ahead, dq, Ps >= kBN ? kBN : Ps, lane, abort, a.err)) {
           alive = false;
           break;
         }
+        if (j % kXWarps != xi) continue;
       }
+      const int st = j % kStages;
       if (!mbar_wait(&sm.kv_full[st], (j / kStages) & 1, abort, a.err)) {
         alive = false;
         break;
       }
       const uint64_t bits = j < kMaxMaskTiles ? sm.tmask[j] : tile_mask<kDense>(a, sm.kept, t0 + j);
       const uint32_t kbase = smem_u32(&sm.k[st][0]), vbase = smem_u32(&sm.v[st][0]);
-      // S^T: this warp's 16 slots x 8 queries
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      // S^T: 64 slots (four groups of 16) x 8 queries
+      float sc[4][4];
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t ka[4];
-        ldsm_x4(sw_addr(kbase, xi * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * kk + (lane >> 4)),
-                ka[0], ka[1], ka[2], ka[3]);
-        mma_16816(sc, ka, qb[kk][0], qb[kk][1]);
+      for (int sg = 0; sg < 4; ++sg) {
+        sc[sg][0] = sc[sg][1] = sc[sg][2] = sc[sg][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t ka[4];
+          ldsm_x4(sw_addr(kbase, sg * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * kk + (lane >> 4)),
+                  ka[0], ka[1], ka[2], ka[3]);
+          mma_16816(sc[sg], ka, qb[kk][0], qb[kk][1]);
+        }
       }
-      // mask, scale, per-query max over the warp's slots
+      // mask, scale, per-query max over the tile's slots
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const bool ok = (bits >> (xi * 16 + g + (e >> 1) * 8)) & 1ull;
-        sc[e] = ok ? sc[e] * sl2 : -INFINITY;
-        mx[e & 1] = fmaxf(mx[e & 1], sc[e]);
-      }
+      for (int sg = 0; sg < 4; ++sg)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const bool ok = (bits >> (sg * 16 + g + (e >> 1) * 8)) & 1ull;
+          sc[sg][e] = ok ? sc[sg][e] * sl2 : -INFINITY;
+          mx[e & 1] = fmaxf(mx[e & 1], sc[sg][e]);
+        }
       float alpha[2], m_use[2];
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
@@ -1141,23 +1153,26 @@ __global__ void __launch_bounds__(tc_threads<MT, EXTRA, FP8>(), 1)
         ox[dt][2] *= alpha[0];
         ox[dt][3] *= alpha[1];
       }
-      // P^T, then O^T += V^T P^T over the warp's 16 slots
-      const float p0 = fast_exp2(sc[0] - m_use[0]);
-      const float p1 = fast_exp2(sc[1] - m_use[1]);
-      const float p2 = fast_exp2(sc[2] - m_use[0]);
-      const float p3 = fast_exp2(sc[3] - m_use[1]);
-      l_x[0] += p0 + p2;
-      l_x[1] += p1 + p3;
-      // (slot g | g+8, query 2tq..) pairs -> transposed: (query g, slots 2tq..)
-      uint32_t pb0 = pack_bf16(p0, p1), pb1 = pack_bf16(p2, p3);
-      asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %0;\n" : "+r"(pb0));
-      asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %0;\n" : "+r"(pb1));
+      // P^T of each slot group, then O^T += V^T P^T over the group's 16 slots
 #pragma unroll
-      for (int dt = 0; dt < 4; ++dt) {
-        uint32_t va[4];
-        ldsm_x4_t(sw_addr(vbase, xi * 16 + (lane & 7) + (lane >> 4) * 8, 2 * dt + ((lane >> 3) & 1)),
-                  va[0], va[1], va[2], va[3]);
-        mma_16816(ox[dt], va, pb0, pb1);
+      for (int sg = 0; sg < 4; ++sg) {
+        const float p0 = fast_exp2(sc[sg][0] - m_use[0]);
+        const float p1 = fast_exp2(sc[sg][1] - m_use[1]);
+        const float p2 = fast_exp2(sc[sg][2] - m_use[0]);
+        const float p3 = fast_exp2(sc[sg][3] - m_use[1]);
+        l_x[0] += p0 + p2;
+        l_x[1] += p1 + p3;
+        // (slot g | g+8, query 2tq..) pairs -> transposed: (query g, slots 2tq..)
+        uint32_t pb0 = pack_bf16(p0, p1), pb1 = pack_bf16(p2, p3);
+        asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %0;\n" : "+r"(pb0));
+        asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %0;\n" : "+r"(pb1));
+#pragma unroll
+        for (int dt = 0; dt < 4; ++dt) {
+          uint32_t va[4];
+          ldsm_x4_t(sw_addr(vbase, sg * 16 + (lane & 7) + (lane >> 4) * 8, 2 * dt + ((lane >> 3) & 1)),
+                    va[0], va[1], va[2], va[3]);
+          mma_16816(ox[dt], va, pb0, pb1);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.kv_empty[st]);
