@@ -30,15 +30,18 @@
 //                tile and when the row's sum would exceed 2^64), writes P =
 //                2^(S - m) as bf16 into TMEM, where PV takes its A operand, and at
 //                the end reads O from TMEM.
-//   warps 0, 12-14  the extra rows (at most 8, if any), one 16-slot quarter of
-//                every tile per warp, through warp-level mma.sync tiles held in
-//                registers; an M = 128 tensor-core tile for 6 rows would cost as
-//                much as a full one.
+//   warps 0, 12-14  the extra rows (at most 8, if any), every fourth tile per
+//                warp, through warp-level mma.sync tiles held in registers; an
+//                M = 128 tensor-core tile for 6 rows would cost as much as a
+//                full one.
+//   FP8 pages    a staging ring of codes and row exponents, dequantized into the
+//                bf16 ring by one more warp and either the producer (no extra
+//                rows) or three of the extra-row warps.
 // With three S buffers per M-tile (P written in place), QK of tile j+3 is
 // issued as soon as the softmax releases tile j, and PV of tile j runs while the
-// softmax works on tile j+1; the softmax and the tensor-core queue set the pace. Every mbarrier wait is bounded; a wait that gives up sets the device
-// error word, and the CTA drains its copies and MMAs and frees TMEM before
-// returning.
+// softmax works on tile j+1; the softmax and the tensor-core queue set the pace.
+// Every mbarrier wait is bounded; a wait that gives up sets the device error
+// word, and the CTA drains its copies and MMAs and frees TMEM before returning.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
