@@ -243,6 +243,28 @@ def test_long_stream_keyframes_24_layers():
     pr.gpu.sync()
 
 
+@pytest.mark.parametrize("ps", [16, 32])
+def test_extra_rows_with_small_pages(ps):
+    """Chunks of 2 frames of 131 tokens, i.e. 262 queries (two M-tiles plus extra
+    rows, each extra-row warp on whole tiles), on pages of 16 and 32 slots, so that
+    a 64-slot tile spans four or two page blocks; 3 chunks visible, every row."""
+    w = WORKLOADS["chunked"].with_(page_size=ps, chunk_size=2, tokens_per_frame=131, sliding_window_num=3,
+                                   heads=2, frames=10)
+    pr = Pair(w, seed=6, pool_pages=128)
+    sid = pr.open()
+    for c in range(5):
+        frames = [2 * c, 2 * c + 1]
+        for f in frames:
+            pr.append(sid, f)
+        pr.check_meta(sid)
+        out = pr.gpu.attend_chunked(pr.gpu_q_chunk(sid, 0, frames), sid, 0, sm_scale=w.sm_scale)
+        o, e = pr.oracle_attention(sid, 0, pr.cpu_q(sid, 0, frames))
+        assert_close(out, o, e, f"page {ps} chunk {c}")
+        pr.evict(sid)
+    pr.check_pool(sid)
+    pr.gpu.sync()
+
+
 def test_chunked_vggt_stream():
     """RFC chunked sliding-window attention: 64 chunks of 8 x 1374 tokens, 4
     chunks visible; tables every chunk, attention of chunks 0-2 and 63 on every
