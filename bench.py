@@ -58,6 +58,8 @@ def parse():
                    help="run N frames of the 24-layer keyframe stream once and exit (a small case for ncu)")
     p.add_argument("--profile-append", type=int, default=0,
                    help="run N batched 32-stream appends (sources rotated over 8 sets) and exit")
+    p.add_argument("--profile-batched", type=int, default=0,
+                   help="N batched attention calls of 32 LingBot-shaped streams (for profiling)")
     p.add_argument("--fp8", action="store_true", help="with --profile-long: E4M3 pages")
     p.add_argument("--no-extra", action="store_true", help="skip the extra workload measurements")
     return p.parse_args()
@@ -1194,10 +1196,21 @@ def run_profile_append(args):
     print(json.dumps({"profile_append": args.profile_append}))
 
 
+def run_profile_batched(args):
+    """N batched attention calls of 32 LingBot-shaped streams at steady state
+    (then the same number of rounds of 32 separate calls)."""
+    import __graft_entry__
+    __graft_entry__.build()
+    extra_multistream(reps=max(args.profile_batched - 3, 1))
+    print(json.dumps({"profile_batched": args.profile_batched}))
+
+
 def main():
     args = parse()
     if args.profile_long:
         run_profile_long(args)
+    elif args.profile_batched:
+        run_profile_batched(args)
     elif args.profile_append:
         run_profile_append(args)
     elif args.profile_frame_attn:

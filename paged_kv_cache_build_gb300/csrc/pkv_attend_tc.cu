@@ -1301,14 +1301,16 @@ int attend_tc_shape(int n_q) {
 int attend_tc_mgroups(int n_q) { return tc_shape(n_q).n_mgroups; }
 
 int attend_tc_splits_pairs(int pairs, int n_tiles, int num_sms) {
-  // a wave's time is proportional to the tiles each CTA handles
+  // a wave's time is the tiles each CTA handles plus a CTA's fixed cost (set-up,
+  // the first tile's cold start, epilogue), ~14 tile periods on a LingBot frame
+  constexpr double kCtaFixedTiles = 14.0;
   int best = 1;
   double best_eff = 0.0;
   for (int s = 1; s <= 16; ++s) {
     if (s > 1 && n_tiles / s < 3) break;
     const int ctas = pairs * s;
     const int waves = (ctas + num_sms - 1) / num_sms;
-    const double t = (double)waves * ((double)n_tiles / s);
+    const double t = (double)waves * ((double)n_tiles / s + kCtaFixedTiles);
     const double eff = (double)pairs * n_tiles / (t * num_sms);
     if (eff > best_eff * 1.03) {
       best_eff = eff;
