@@ -77,8 +77,9 @@ def test_noalloc_matches_attend_twice(lib, name, frames):
 
 
 def test_noalloc_rejects_more_than_its_scratch(lib):
-    """A whole chunk of 8 x 1374 queries needs more split-KV scratch than the
-    fixed 16 MiB: the call refuses, launches nothing, and pkv_attend still works."""
+    """A whole chunk of 8 x 1374 queries over the full window of 4 chunks (687
+    tiles, 3 KV splits) needs more split-KV scratch than the fixed 16 MiB: the
+    call refuses, launches nothing, and pkv_attend still works."""
     from paged_kv_cache_build_gb300 import PagedKVCache, chunked_stream_cfg
     w = WORKLOADS["chunked"]
     cache = PagedKVCache(w.pool_pages, w.page_size, w.heads, w.head_dim)
@@ -86,8 +87,11 @@ def test_noalloc_rejects_more_than_its_scratch(lib):
     kv = torch.empty((w.chunk_size, w.tokens_per_frame, w.heads, w.head_dim), dtype=torch.bfloat16,
                      device="cuda")
     _fill(kv, w, sid, 0, TENSOR_K)
-    for f in range(w.chunk_size):
-        cache.append_frame(sid, kv[f], kv[f])
+    for c in range(w.sliding_window_num):
+        for f in range(w.chunk_size):
+            cache.append_frame(sid, kv[f], kv[f])
+        if c < w.sliding_window_num - 1:
+            cache.evict_window(sid)
     n_q = w.chunk_size * w.tokens_per_frame
     q = torch.zeros((n_q, w.heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
     out = torch.zeros_like(q)
