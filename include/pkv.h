@@ -420,8 +420,9 @@ pkv_status pkv_attend_batched(pkv_t h, const void* q, const int* q_off, const in
  * cudaFree imply, and hosts whose device memory belongs to another allocator. They
  * can create the handle and open the stream up front and then call this.
  *  - A call whose partial results need more than 16 MiB (num_splits x n_q x heads
- *    x 264 bytes; e.g. a whole 8 x 1374-token chunk) returns PKV_ERR_INVALID and
- *    launches nothing.
+ *    x 264 bytes; e.g. a whole 8 x 1374-token chunk over a window of 4 chunks,
+ *    which runs in 3 KV splits) returns PKV_ERR_INVALID and launches nothing. The
+ *    split count follows the call's shape (a call that runs unsplit needs none).
  *  - pkv_create_ex resolves the array's device address (cudaGetSymbolAddress,
  *    no allocation) for the device current at creation, which is the handle's
  *    device; a handle created after a device reset resolves it again. So the
